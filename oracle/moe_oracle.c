@@ -1,0 +1,330 @@
+/*
+ * moe_oracle.c -- CPU oracle for the MoE expert-parallel dispatch/combine path.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+ * and the benchmark's CPU-baseline/reference leg load this file's library.  The
+ * CUDA library never calls it, and the two share no code, headers or tables.
+ *
+ * Plain, single-threaded C99, compiled with -ffp-contract=off so that every
+ * float operation is one IEEE-754 single-precision operation rounded to nearest.
+ * Each function states the passage it follows.  Pins (what each function is
+ * checked against, independently of itself) live in tests/test_oracle_*.py:
+ *
+ *   oracle_layout          numpy bincount / cumsum / stable argsort, O(N^2) brute force
+ *   oracle_dispatch        row equality against the stable argsort permutation
+ *   oracle_e4m3_encode     torch float8_e4m3fn cast of saturated inputs, all codes
+ *   oracle_dispatch_quant  encoder pin + per-block invariants (amax -> +-448, dequant
+ *                          error bound, zero block); the scale recipe itself is a
+ *                          reading: the pages only name W8A8 (parity unpinned against
+ *                          the pages for the recipe, pinned for the arithmetic)
+ *   oracle_combine         float64 closed form within the fp32 error bound, one-hot
+ *                          weights, identity-expert round trip
+ *   oracle_f32_to_bf16     torch bfloat16 cast
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_INVALID_ARG 1
+#define ORACLE_ERR_BAD_INDEX 2
+
+/* ------------------------------------------------------------------------- */
+/* bf16 <-> f32                                                               */
+/* ------------------------------------------------------------------------- */
+
+/* bf16 is the upper half of an IEEE binary32 word: widening is exact. */
+static float bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round binary32 to bf16, nearest with ties to even; NaN stays a quiet NaN. */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lower = u & 0xFFFFu;
+    uint32_t upper = u >> 16;
+    /* round up when the dropped half is above one half, or exactly one half
+       and the kept part is odd */
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u;
+    return (uint16_t)upper;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Layout: count -> exclusive scan -> stable slot map                         */
+/* UBEP, section 2.3 / Figure 2 (dispatch phases: per-expert token counts,    */
+/* then offsets and contiguous per-expert reordering) and section 4 (receive  */
+/* region pre-partitioned by source and expert); StrataCL, Appendix D (first  */
+/* level: destination expert, per-expert counts, prefix-sum offsets and       */
+/* token-local offsets).  Order inside an expert: source token, then k slot.  */
+/* ------------------------------------------------------------------------- */
+int oracle_layout(int T, int k, int E, int R, const int32_t *topk_idx,
+                  int32_t *expert_counts, int32_t *expert_offsets,
+                  int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of)
+{
+    if (T < 0 || k < 1 || E < 1 || R < 1 || E % R != 0)
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    const int El = E / R;
+
+    /* 1. count: how many (token, slot) pairs chose each expert */
+    for (int e = 0; e < E; ++e)
+        expert_counts[e] = 0;
+    for (int64_t i = 0; i < N; ++i) {
+        int e = topk_idx[i];
+        if (e < 0 || e >= E)
+            return ORACLE_ERR_BAD_INDEX;
+        expert_counts[e] += 1;
+    }
+
+    /* 2. exclusive prefix sum over experts; experts of rank r are the
+          contiguous block r*El .. r*El+El-1, so rank offsets are a subsample */
+    expert_offsets[0] = 0;
+    for (int e = 0; e < E; ++e)
+        expert_offsets[e + 1] = expert_offsets[e] + expert_counts[e];
+    for (int r = 0; r <= R; ++r)
+        rank_offsets[r] = expert_offsets[r * El];
+
+    /* 3. walk (token, slot) pairs in lexicographic order; each expert hands
+          out its slots in that order */
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+    if (!cursor)
+        return ORACLE_ERR_INVALID_ARG;
+    for (int e = 0; e < E; ++e)
+        cursor[e] = expert_offsets[e];
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t i = (int64_t)t * k + j;
+            int e = topk_idx[i];
+            int32_t s = cursor[e]++;
+            slot_of[i] = s;
+            src_of[s] = (int32_t)i;
+        }
+    }
+    free(cursor);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Dispatch (bf16): every token row goes, unchanged, to each of its k slots.  */
+/* UBEP section 2.3 (Phase 2: a token may be sent to several experts);        */
+/* RailWave section 3.2 (payload packed without padding).                     */
+/* ------------------------------------------------------------------------- */
+int oracle_dispatch(int T, int H, int k, const uint16_t *x, const int32_t *slot_of,
+                    uint16_t *recv)
+{
+    if (T < 0 || H < 1 || k < 1)
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int32_t s = slot_of[(int64_t)t * k + j];
+            if (s < 0 || s >= N)
+                return ORACLE_ERR_BAD_INDEX;
+            memcpy(recv + (int64_t)s * H, x + (int64_t)t * H, sizeof(uint16_t) * (size_t)H);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP8 E4M3 encoding, written from the OCP 8-bit floating point definition:   */
+/* 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; no infinities;   */
+/* S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448;    */
+/* subnormals (exponent field 0) are m * 2^-9.  Rounding: nearest, ties to    */
+/* even; "satfinite": magnitudes beyond 448 (and infinities) clamp to 448.    */
+/* ------------------------------------------------------------------------- */
+uint8_t oracle_e4m3_encode(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint8_t sign = (uint8_t)((u >> 31) << 7);
+    if (isnan(f))
+        return (uint8_t)(sign | 0x7F);
+    double a = fabs((double)f);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    if (a == 0.0)
+        return sign;
+    int e2;
+    (void)frexp(a, &e2); /* a = m * 2^e2 with m in [0.5, 1) */
+    int e = e2 - 1;      /* a = (1 + frac) * 2^e               */
+    uint32_t code;
+    if (e < -6) {
+        /* subnormal: count steps of 2^-9, rounded half to even */
+        double steps = ldexp(a, 9);          /* exact: power-of-two scale */
+        double r = nearbyint(steps);         /* default mode: ties to even */
+        code = (uint32_t)r;                  /* r == 8 is the smallest normal, code 0x08 */
+    } else {
+        double frac8 = (ldexp(a, -e) - 1.0) * 8.0; /* exact: 24-bit significand */
+        double r = nearbyint(frac8);
+        int ee = e;
+        if (r == 8.0) {
+            r = 0.0;
+            ee += 1;
+        }
+        code = ((uint32_t)(ee + 7) << 3) | (uint32_t)r;
+        if (code > 0x7Eu)
+            code = 0x7Eu;
+    }
+    return (uint8_t)(sign | code);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Dispatch with fused FP8 quantisation (UBEP Table 3: DeepSeek-R1/V3.2 run    */
+/* W8A8; the pages give no more than that).  Reading used here: 1 x 128 blocks */
+/* along H per token row; amax = max |x|; scale = amax / 448; the codes are    */
+/* e4m3_satfinite(x * (448 / amax)), both quotients rounded to nearest once.  */
+/* A block with amax == 0, or whose 448 / amax overflows binary32, stores      */
+/* scale 1 and signed zero codes.  Scales are float32 row-major [N, H/128].    */
+/* The same codes and scale go to every one of the token's k slots.           */
+/* ------------------------------------------------------------------------- */
+int oracle_dispatch_quant(int T, int H, int k, const uint16_t *x, const int32_t *slot_of,
+                          uint8_t *recv_q, float *recv_scales)
+{
+    if (T < 0 || H < 128 || H % 128 != 0 || k < 1)
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    const int B = H / 128;
+    uint8_t *qrow = (uint8_t *)malloc((size_t)H);
+    float *srow = (float *)malloc(sizeof(float) * (size_t)B);
+    if (!qrow || !srow) {
+        free(qrow);
+        free(srow);
+        return ORACLE_ERR_INVALID_ARG;
+    }
+    for (int t = 0; t < T; ++t) {
+        const uint16_t *xr = x + (int64_t)t * H;
+        for (int b = 0; b < B; ++b) {
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                float v = fabsf(bf16_to_f32(xr[b * 128 + i]));
+                if (v > amax)
+                    amax = v;
+            }
+            float inv = 0.0f;
+            int zero_block = (amax == 0.0f);
+            if (!zero_block) {
+                inv = 448.0f / amax;
+                if (isinf(inv))
+                    zero_block = 1;
+            }
+            if (zero_block) {
+                srow[b] = 1.0f;
+                for (int i = 0; i < 128; ++i)
+                    qrow[b * 128 + i] = (uint8_t)((xr[b * 128 + i] >> 15) << 7);
+            } else {
+                srow[b] = amax / 448.0f;
+                for (int i = 0; i < 128; ++i) {
+                    float v = bf16_to_f32(xr[b * 128 + i]);
+                    float p = v * inv;
+                    qrow[b * 128 + i] = oracle_e4m3_encode(p);
+                }
+            }
+        }
+        for (int j = 0; j < k; ++j) {
+            int32_t s = slot_of[(int64_t)t * k + j];
+            if (s < 0 || s >= N) {
+                free(qrow);
+                free(srow);
+                return ORACLE_ERR_BAD_INDEX;
+            }
+            memcpy(recv_q + (int64_t)s * H, qrow, (size_t)H);
+            memcpy(recv_scales + (int64_t)s * B, srow, sizeof(float) * (size_t)B);
+        }
+    }
+    free(qrow);
+    free(srow);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Combine: out[t,:] = sum_j w[t,j] * y[slot_of[t,j], :]                       */
+/* HyperParallel-MoE section 2.2 (outputs weighted by routing scores and       */
+/* combined; Combine accumulates the top-k contributions) and section 4.1     */
+/* (contributions accumulated according to routing scores); RailWave section  */
+/* 3 (combine uses the saved dispatch metadata to return rows to their token  */
+/* positions).  Precision: fp32 accumulation, one fused multiply-add per slot, */
+/* slots in order j = 0..k-1, starting from +0; output rounded once.           */
+/* out_dtype: 0 = bf16 bits (uint16), 1 = float32.                            */
+/* ------------------------------------------------------------------------- */
+int oracle_combine(int T, int H, int k, const uint16_t *y, const int32_t *slot_of,
+                   const float *topk_w, void *out, int out_dtype)
+{
+    if (T < 0 || H < 1 || k < 1 || (out_dtype != 0 && out_dtype != 1))
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int32_t s = slot_of[(int64_t)t * k + j];
+            if (s < 0 || s >= N)
+                return ORACLE_ERR_BAD_INDEX;
+        }
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                int64_t i = (int64_t)t * k + j;
+                float v = bf16_to_f32(y[(int64_t)slot_of[i] * H + h]);
+                acc = fmaf(topk_w[i], v, acc);
+            }
+            if (out_dtype == 0)
+                ((uint16_t *)out)[(int64_t)t * H + h] = oracle_f32_to_bf16(acc);
+            else
+                ((float *)out)[(int64_t)t * H + h] = acc;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* The same weighted sum in binary64 (products of a binary32 weight and a bf16
+   value are exact in binary64).  Used as the closed-form pin of oracle_combine. */
+int oracle_combine_f64(int T, int H, int k, const uint16_t *y, const int32_t *slot_of,
+                       const float *topk_w, double *out, double *abs_sum)
+{
+    if (T < 0 || H < 1 || k < 1)
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    for (int t = 0; t < T; ++t) {
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0, mag = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int64_t i = (int64_t)t * k + j;
+                int32_t s = slot_of[i];
+                if (s < 0 || s >= N)
+                    return ORACLE_ERR_BAD_INDEX;
+                double p = (double)topk_w[i] * (double)bf16_to_f32(y[(int64_t)s * H + h]);
+                acc += p;
+                mag += fabs(p);
+            }
+            out[(int64_t)t * H + h] = acc;
+            if (abs_sum)
+                abs_sum[(int64_t)t * H + h] = mag;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Array forms of the two encoders, for exhaustive sweeps in the tests. */
+void oracle_e4m3_encode_array(const float *f, uint8_t *q, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        q[i] = oracle_e4m3_encode(f[i]);
+}
+
+void oracle_f32_to_bf16_array(const float *f, uint16_t *b, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        b[i] = oracle_f32_to_bf16(f[i]);
+}
+
+int oracle_abi_version(void) { return 1; }

@@ -1,0 +1,80 @@
+"""The oracle's pins have teeth: each plausible mistake, planted in a temporary
+copy of the oracle's C source on the CPU, makes at least one pin fail."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_combine as tc
+import test_oracle_dispatch as td
+import test_oracle_layout as tl
+import test_oracle_bf16 as tb
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    # layout: walk the k slots backwards (unstable inside a token)
+    "slot_order": ("for (int j = 0; j < k; ++j) {\n            int64_t i = (int64_t)t * k + j;\n            int e = topk_idx[i];\n            int32_t s = cursor[e]++;",
+                   "for (int j = k - 1; j >= 0; --j) {\n            int64_t i = (int64_t)t * k + j;\n            int e = topk_idx[i];\n            int32_t s = cursor[e]++;"),
+    # layout: rank offsets indexed by rank instead of first expert of the rank
+    "rank_index": ("rank_offsets[r] = expert_offsets[r * El];", "rank_offsets[r] = expert_offsets[r];"),
+    # layout: each expert starts at the previous expert's offset (scan shifted by one)
+    "shifted_scan": ("cursor[e] = expert_offsets[e];", "cursor[e] = e > 0 ? expert_offsets[e - 1] : 0;"),
+    # e4m3: ties away from zero
+    "e4m3_ties": ("double r = nearbyint(frac8);", "double r = round(frac8);"),
+    # e4m3: exponent bias 8
+    "e4m3_bias": ("code = ((uint32_t)(ee + 7) << 3) | (uint32_t)r;", "code = ((uint32_t)(ee + 8) << 3) | (uint32_t)r;"),
+    # quant: scale divisor off (E5M2's max instead of E4M3's)
+    "quant_scale": ("srow[b] = amax / 448.0f;", "srow[b] = amax / 57344.0f;"),
+    # combine: the slot index dropped (always slot 0 of the token)
+    "combine_index": ("float v = bf16_to_f32(y[(int64_t)slot_of[i] * H + h]);",
+                      "float v = bf16_to_f32(y[(int64_t)slot_of[(int64_t)t * k] * H + h]);"),
+    # combine: weight and value of neighbouring slots swapped
+    "combine_weight": ("acc = fmaf(topk_w[i], v, acc);", "acc = fmaf(topk_w[(int64_t)t * k + (j + 1) % k], v, acc);"),
+    # bf16: ties rounded up instead of to even
+    "bf16_ties": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (lower >= 0x8000u)"),
+}
+
+
+def _pins():
+    lay = tl.CASES
+    pins = []
+    for c in lay[:8]:
+        pins += [lambda c=c: tl.test_counts_and_offsets_match_library(*c),
+                 lambda c=c: tl.test_slot_map_is_stable_counting_sort(*c),
+                 lambda c=c: tl.test_rank_segments_hold_their_experts(*c)]
+    pins += [tl.test_hand_worked_example, tl.test_duplicate_expert_in_one_token,
+             td.test_e4m3_every_code_round_trips, td.test_e4m3_midpoints_and_neighbours_match_torch,
+             td.test_quant_zero_and_tiny_blocks, td.test_dispatch_hand_worked,
+             lambda: td.test_quant_block_invariants(("fuzz", 0)),
+             lambda: td.test_dispatch_rows_equal_source_token(("fuzz", 0)),
+             tc.test_one_hot_weights_select_one_slot, tc.test_weights_are_not_renormalised,
+             lambda: tc.test_bf16_output_is_rounded_fp32_output("fuzz0", None),
+             tb.test_random_and_special_values_match_torch]
+    return pins
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmutant.so")
+    oracle.compile_to(str(path), so)
+    monkeypatch.setattr(oracle, "_lib", oracle._bind(so))
+    failed = 0
+    for pin in _pins():
+        try:
+            pin()
+        except (AssertionError, oracle.OracleError, IndexError, ValueError):
+            failed += 1
+    assert failed > 0, f"no pin caught mutation {name}"
+
+
+def test_unmutated_oracle_passes_all_pins():
+    for pin in _pins():
+        pin()
