@@ -1,0 +1,472 @@
+"""Benchmark: MoE expert-parallel dispatch + combine on one GB300 (or N replicas).
+
+One step = the whole hot path over one batch: layout (count kernel, scan+assign
+kernel) -> dispatch (bf16 row scatter, or the fused FP8 variant for FP8
+workloads) -> combine (router-weighted fp32 gather-reduce, bf16 out) of
+synthetic expert outputs.  Default workload: DeepSeek-V3-style decode batch,
+T=1024, H=7168, top-8 of E=256 experts on R=32 virtual ranks.
+
+Timing: W untimed warm-up steps, then exactly K timed steps between a barrier
+and a device synchronisation.  Before every step a 2xL2-sized buffer is
+written (L2 flush); CUDA events on the launching stream bracket each kernel,
+so the flush is outside the measured step time.  value = tokens per second over
+all ranks (weak scaling: each rank runs its own replica).  `e2e` repeats the
+step through the public API with the inputs copied from pinned host memory and
+the combined output copied back, inside the timed region.
+
+--impl reference times the CPU oracle (the plain C statement of the method) on
+the same metric: every step is a bounded sample of the same workload recipe.
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "dsv3_decode"
+
+
+# ------------------------------------------------------------------ bytes
+
+def kernel_bytes(name: str, T: int, H: int, k: int, E: int, R: int = 1) -> int:
+    """Algorithmic bytes one launch must move (HBM reads + writes), per kernel.
+
+    layout_count   reads topk_idx once
+    layout_assign  reads topk_idx, writes slot_of and src_of, counts and offsets
+    dispatch_bf16  reads x and slot_of once, writes k copies of every row
+    dispatch_fp8   reads x and slot_of, writes k copies of the codes and scales
+    combine        reads k rows per token, slot_of and weights, writes one row
+    """
+    N = T * k
+    if name == "layout_count":
+        return 4 * N
+    if name == "layout_assign":
+        return 12 * N + 4 * (2 * E + 1 + R + 1)
+    if name == "dispatch_bf16":
+        return 2 * T * H + 4 * N + 2 * N * H
+    if name == "dispatch_fp8":
+        return 2 * T * H + 4 * N + N * H + 4 * N * (H // 128)
+    if name == "combine":
+        return 2 * N * H + 8 * N + 2 * T * H
+    raise KeyError(name)
+
+
+def step_bytes(T, H, k, E, R, fp8: bool) -> int:
+    d = "dispatch_fp8" if fp8 else "dispatch_bf16"
+    return sum(kernel_bytes(n, T, H, k, E, R)
+               for n in ("layout_count", "layout_assign", d, "combine"))
+
+
+# ------------------------------------------------------------------ host helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def allreduce_max(x: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi; summary() keeps
+    only the samples taken between mark_start() and mark_stop()."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+        self._t = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            deadline = time.perf_counter() + 5.0
+            while not self.lines and time.perf_counter() < deadline and self.proc.poll() is None:
+                time.sleep(0.02)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_stop(self):
+        self.t1 = time.perf_counter()
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for ts, ln in self.lines:
+            if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
+                continue
+            p = [c.strip() for c in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, p[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_smi_id(torch, dev) -> str:
+    """nvidia-smi id of a torch device (its UUID when torch exposes it)."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+def measured_peak_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if that kernel's
+    source is unchanged since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+        src = os.path.join(ROOT, rec["source"])
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if sha != rec["source_sha256"]:
+            return None
+        return rec
+    except (OSError, KeyError, ValueError, TypeError, AttributeError):
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_step(w, y_np, fp8: bool):
+    import oracle
+    counts, offs, roffs, slot_of, src_of = oracle.layout(w.topk_idx, w.E, w.R)
+    if fp8:
+        oracle.dispatch_quant(w.x, slot_of)
+    else:
+        oracle.dispatch(w.x, slot_of)
+    oracle.combine(y_np, slot_of, w.topk_w, "bf16")
+
+
+def cpu_baseline(name: str, budget_s: float = 12.0):
+    """The oracle on the host, single-threaded, over whole steps of the workload
+    until `budget_s` of CPU work (at least one step)."""
+    from workloads.gen import make_workload, expert_output, CONFIGS
+    w = make_workload(name)
+    y = expert_output(w.N, w.H, seed=w.seed)
+    fp8 = CONFIGS[name]["payload"] == "fp8"
+    _ = w.x
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(w, y, fp8)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": steps * w.T / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{steps} whole {name} steps (T={w.T}: layout + "
+                      f"{'fp8 ' if fp8 else ''}dispatch + combine), single-threaded C, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads.gen import make_workload, expert_output, CONFIGS
+    name = args.config
+    full = CONFIGS[name]["T"]
+    Ts = max(1, min(full, args.ref_tokens))
+    w = make_workload(name, T=Ts)
+    y = expert_output(w.N, w.H, seed=w.seed)
+    fp8 = CONFIGS[name]["payload"] == "fp8"
+    _ = w.x
+    for _ in range(args.warmup):
+        oracle_step(w, y, fp8)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, y, fp8)
+    el = time.perf_counter() - t0
+    value = args.steps * Ts / el
+    c = CONFIGS[name]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 + bf16" if fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": f"{name} T={c['T']} H={c['H']} k={c['k']} E={c['E']} R={c['R']}",
+                   "sample_tokens_per_step": Ts},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the {name} recipe at T={Ts} tokens "
+                                   f"(layout + {'fp8 ' if fp8 else ''}dispatch + combine)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import combine_layout_moe_gb300 as m
+    from workloads.gen import make_workload, expert_output, CONFIGS
+
+    name = args.config
+    c = CONFIGS[name]
+    fp8 = c["payload"] == "fp8"
+    w = make_workload(name, seed=args.seed + rank)
+    T, H, k, E, R, N = w.T, w.H, w.k, w.E, w.R, w.N
+
+    # inputs resident in HBM
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    idx = torch.from_numpy(w.topk_idx).to(dev)
+    wt = torch.from_numpy(w.topk_w).to(dev)
+    y = torch.from_numpy(expert_output(N, H, seed=w.seed).view(np.int16)).to(dev).view(torch.bfloat16)
+    err = m.new_error_word(dev)
+    ws = torch.empty(m.moe_layout_workspace_bytes(T, k, E), dtype=torch.uint8, device=dev)
+    lay = m.Layout(torch.empty(E, dtype=torch.int32, device=dev),
+                   torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   torch.empty(R + 1, dtype=torch.int32, device=dev),
+                   torch.empty((T, k), dtype=torch.int32, device=dev),
+                   torch.empty(T * k, dtype=torch.int32, device=dev))
+    if fp8:
+        recv_q = torch.empty((N, H), dtype=torch.uint8, device=dev)
+        recv_s = torch.empty((N, H // 128), dtype=torch.float32, device=dev)
+    else:
+        recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def layout_only():
+        m.moe_layout(idx, E, R, workspace=ws, err_word=err, out=lay, stream=stream)
+
+    def dispatch_only():
+        if fp8:
+            m.moe_dispatch_quant(x, lay.slot_of, recv_q=recv_q, recv_scales=recv_s,
+                                 err_word=err, stream=stream)
+        else:
+            m.moe_dispatch(x, lay.slot_of, recv=recv, err_word=err, stream=stream)
+
+    def combine_only():
+        m.moe_combine(y, lay.slot_of, wt, out=out, err_word=err, stream=stream)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(events=None):
+        flush.fill_(0)
+        if events:
+            events[0].record(stream)
+        layout_only()
+        if events:
+            events[1].record(stream)
+        dispatch_only()
+        if events:
+            events[2].record(stream)
+        combine_only()
+        if events:
+            events[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bits = m.moe_read_error(err)
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x} during warm-up")
+
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_smi_id(torch, dev)) as clocks:
+        clocks.mark_start()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step(ev[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        clocks.mark_stop()
+    barrier()
+    t_layout = [e[0].elapsed_time(e[1]) for e in ev]
+    t_disp = [e[1].elapsed_time(e[2]) for e in ev]
+    t_comb = [e[2].elapsed_time(e[3]) for e in ev]
+    t_step = [e[0].elapsed_time(e[3]) for e in ev]
+    total_ms = allreduce_max(sum(t_step))
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1000.0)
+
+    # per-kernel view of the dominant kernel (dispatch or combine) and roofline
+    d_name = "dispatch_fp8" if fp8 else "dispatch_bf16"
+    avg_d, avg_c = statistics.mean(t_disp), statistics.mean(t_comb)
+    dom, dom_ms = (d_name, avg_d) if avg_d >= avg_c else ("combine", avg_c)
+    dom_bytes = kernel_bytes(dom, T, H, k, E, R)
+    peak, peak_kind = measured_peak_gbs()
+    achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
+    kern_name = {"dispatch_bf16": "dispatch_bf16_kernel", "dispatch_fp8": "dispatch_fp8_kernel",
+                 "combine": "combine_kernel"}[dom]
+    tr = recorded_traffic(kern_name)
+    traffic = None
+    if tr is not None and tr.get("workload") == name:
+        traffic = tr.get("dram_bytes_per_launch")
+
+    # e2e through the public API: pinned host inputs in, combined output back
+    x_h = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    idx_h = torch.from_numpy(w.topk_idx).pin_memory()
+    wt_h = torch.from_numpy(w.topk_w).pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 3):
+        flush.fill_(0)
+        e = ee[i - 3] if i >= 3 else None
+        if e:
+            e[0].record(stream)
+        x.copy_(x_h, non_blocking=True)
+        idx.copy_(idx_h, non_blocking=True)
+        wt.copy_(wt_h, non_blocking=True)
+        layout_only()
+        dispatch_only()
+        combine_only()
+        out_h.copy_(out, non_blocking=True)
+        if e:
+            e[1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = allreduce_max(sum(a.elapsed_time(b) for a, b in ee)) / e2e_steps
+    bits = m.moe_read_error(err)
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x}")
+    h2d = x.numel() * 2 + idx.numel() * 4 + wt.numel() * 4
+    d2h = out.numel() * 2
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 + bf16" if fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": f"{name} T={T} H={H} k={k} E={E} R={R}",
+                   "tokens_per_step": T, "l2": "flushed before every step (2xL2 write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": kern_name, "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes},
+        "kernels_ms": {"layout": statistics.mean(t_layout), d_name: avg_d, "combine": avg_c},
+        "step_hbm_gbs": step_bytes(T, H, k, E, R, fp8) / (ms_per_step / 1000.0) / 1e9,
+        "wall_ms_per_step_incl_flush": 1000.0 * wall / args.steps,
+        "e2e": {"value": world * T / (e2e_ms / 1000.0), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(name, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default=DEFAULT_WORKLOAD)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--cpu-budget", type=float, default=12.0)
+    p.add_argument("--ref-tokens", type=int, default=64,
+                   help="tokens per oracle step in --impl reference")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+    try:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

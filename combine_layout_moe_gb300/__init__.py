@@ -1,0 +1,215 @@
+"""GB300 MoE expert-parallel layout / dispatch / combine.
+
+A thin ctypes binding over the C ABI of libmoe_ep.so (include/moe_ep.h).  The
+functions carry the C names and only marshal arguments: they check dtypes and
+shapes, allocate outputs with torch when none are given, and pass raw device
+pointers and the current CUDA stream.  Every step of the path runs in the
+library's sm_103a kernels; there is no CPU or PyTorch fallback.  If the
+library is missing, importing this package fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_ep.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_BAD_INDEX, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, \
+    MOE_ERR_UNSUPPORTED = range(6)
+MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
+MOE_ERRBIT_BAD_INDEX, MOE_ERRBIT_TIMEOUT = 0x1, 0x2
+MOE_MAX_EXPERTS = 1024
+
+# Every symbol the header declares, with its ctypes signature.
+_P, _I, _SZ, _U32P = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+SIGNATURES = {
+    "moe_abi_version": ([], ctypes.c_int),
+    "moe_status_string": ([_I], ctypes.c_char_p),
+    "moe_layout_workspace_bytes": ([_I, _I, _I], ctypes.c_size_t),
+    "moe_layout": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P], ctypes.c_int),
+    "moe_dispatch": ([_I, _I, _I, _P, _P, _P, _U32P, _P], ctypes.c_int),
+    "moe_dispatch_quant": ([_I, _I, _I, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
+    "moe_combine": ([_I, _I, _I, _P, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
+    "moe_read_error": ([_U32P, _I, _P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+            "or `python combine_layout_moe_gb300/build.py` first")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _lib.moe_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _want(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def moe_abi_version() -> int:
+    return _lib.moe_abi_version()
+
+
+def moe_status_string(status: int) -> str:
+    return _lib.moe_status_string(status).decode()
+
+
+def new_error_word(device=None) -> torch.Tensor:
+    """A zero-filled device word for the kernels' error bits (int32 storage)."""
+    return torch.zeros(4, dtype=torch.int32, device=device or "cuda")
+
+
+def moe_layout_workspace_bytes(T: int, k: int, E: int) -> int:
+    return int(_lib.moe_layout_workspace_bytes(T, k, E))
+
+
+class Layout(NamedTuple):
+    expert_counts: torch.Tensor   # int32 [E]
+    expert_offsets: torch.Tensor  # int32 [E+1]
+    rank_offsets: torch.Tensor    # int32 [R+1]
+    slot_of: torch.Tensor         # int32 [T, k]
+    src_of: torch.Tensor          # int32 [T*k]
+
+
+def moe_layout(topk_idx: torch.Tensor, E: int, R: int, *, workspace: Optional[torch.Tensor] = None,
+               err_word: Optional[torch.Tensor] = None, out: Optional[Layout] = None,
+               stream: Optional[torch.cuda.Stream] = None) -> Layout:
+    """Count, scan and stable slot map of top-k router output (see moe_ep.h)."""
+    if topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be [T, k]")
+    T, k = topk_idx.shape
+    _want(topk_idx, "topk_idx", torch.int32)
+    dev = topk_idx.device
+    if out is None:
+        out = Layout(torch.empty(E, dtype=torch.int32, device=dev),
+                     torch.empty(E + 1, dtype=torch.int32, device=dev),
+                     torch.empty(R + 1, dtype=torch.int32, device=dev),
+                     torch.empty((T, k), dtype=torch.int32, device=dev),
+                     torch.empty(T * k, dtype=torch.int32, device=dev))
+    need = moe_layout_workspace_bytes(T, k, E)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(_lib.moe_layout(T, k, E, R, _ptr(topk_idx), _ptr(out.expert_counts),
+                           _ptr(out.expert_offsets), _ptr(out.rank_offsets), _ptr(out.slot_of),
+                           _ptr(out.src_of), _ptr(workspace), workspace.numel() *
+                           workspace.element_size(), _ptr(err_word), _stream(stream)),
+           "moe_layout")
+    return out
+
+
+def moe_dispatch(x: torch.Tensor, slot_of: torch.Tensor, *, recv: Optional[torch.Tensor] = None,
+                 err_word: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """recv[slot_of[t, j]] = x[t] (bf16 rows)."""
+    T, H = x.shape
+    k = slot_of.shape[1]
+    _want(x, "x", torch.bfloat16)
+    _want(slot_of, "slot_of", torch.int32, (T, k))
+    if recv is None:
+        recv = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
+    _want(recv, "recv", torch.bfloat16, (T * k, H))
+    _check(_lib.moe_dispatch(T, H, k, _ptr(x), _ptr(slot_of), _ptr(recv), _ptr(err_word),
+                             _stream(stream)), "moe_dispatch")
+    return recv
+
+
+def moe_dispatch_quant(x: torch.Tensor, slot_of: torch.Tensor, *,
+                       recv_q: Optional[torch.Tensor] = None,
+                       recv_scales: Optional[torch.Tensor] = None,
+                       err_word: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None):
+    """Dispatch with fused FP8-E4M3 1x128 block quantisation.
+    Returns (recv_q uint8 [T*k, H], recv_scales float32 [T*k, H/128])."""
+    T, H = x.shape
+    k = slot_of.shape[1]
+    _want(x, "x", torch.bfloat16)
+    _want(slot_of, "slot_of", torch.int32, (T, k))
+    if recv_q is None:
+        recv_q = torch.empty((T * k, H), dtype=torch.uint8, device=x.device)
+    if recv_scales is None:
+        recv_scales = torch.empty((T * k, H // 128), dtype=torch.float32, device=x.device)
+    _want(recv_q, "recv_q", torch.uint8, (T * k, H))
+    _want(recv_scales, "recv_scales", torch.float32, (T * k, H // 128))
+    _check(_lib.moe_dispatch_quant(T, H, k, _ptr(x), _ptr(slot_of), _ptr(recv_q),
+                                   _ptr(recv_scales), _ptr(err_word), _stream(stream)),
+           "moe_dispatch_quant")
+    return recv_q, recv_scales
+
+
+def moe_combine(y: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.Tensor, *,
+                out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+                err_word: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out[t] = sum_j topk_w[t, j] * y[slot_of[t, j]] with fp32 accumulation."""
+    T, k = slot_of.shape
+    H = y.shape[1]
+    _want(y, "y", torch.bfloat16, (T * k, H))
+    _want(slot_of, "slot_of", torch.int32)
+    _want(topk_w, "topk_w", torch.float32, (T, k))
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out_dtype must be bfloat16 or float32")
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=y.device)
+    _want(out, "out", out_dtype, (T, H))
+    code = MOE_OUT_BF16 if out_dtype == torch.bfloat16 else MOE_OUT_F32
+    _check(_lib.moe_combine(T, H, k, _ptr(y), _ptr(slot_of), _ptr(topk_w), _ptr(out), code,
+                            _ptr(err_word), _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_read_error(err_word: torch.Tensor, clear: bool = True,
+                   stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise, read (and clear) the error word; returns the error bits."""
+    bits = ctypes.c_uint32(0)
+    st = _lib.moe_read_error(_ptr(err_word), 1 if clear else 0, _stream(stream),
+                             ctypes.byref(bits))
+    if st == MOE_ERR_CUDA or st == MOE_ERR_INVALID_ARG:
+        _check(st, "moe_read_error")
+    return int(bits.value)
+
+
+__all__ = [
+    "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word",
+    "moe_layout_workspace_bytes", "moe_layout", "moe_dispatch", "moe_dispatch_quant",
+    "moe_combine", "moe_read_error", "LIB_PATH", "SIGNATURES",
+]

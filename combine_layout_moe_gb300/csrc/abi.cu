@@ -1,0 +1,179 @@
+// C ABI entry points of libmoe_ep.so: argument checks, then the launchers.
+// Nothing here allocates device memory or synchronises, except
+// moe_read_error, whose job is to synchronise and read the error word.
+#include <cstdint>
+#include <cstring>
+
+#include "launch.h"
+#include "moe_ep.h"
+
+namespace moe {
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0)
+        return cached[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev >= 0 && dev < 64)
+        cached[dev] = n;
+    return n;
+}
+
+int warp_item_grid(const void *kernel, int threads, size_t smem, int64_t items)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t warps_per_cta = threads / 32;
+    const int64_t need = (items + warps_per_cta - 1) / warps_per_cta;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t g = need < cap ? need : cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace moe
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool pairs_ok(int T, int k)
+{
+    return T >= 0 && k >= 1 && (int64_t)T * k < ((int64_t)1 << 31);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return 1; }
+
+const char *moe_status_string(int status)
+{
+    switch (status) {
+    case MOE_OK:
+        return "ok";
+    case MOE_ERR_INVALID_ARG:
+        return "invalid argument";
+    case MOE_ERR_BAD_INDEX:
+        return "expert id or slot index out of range";
+    case MOE_ERR_CUDA:
+        return "CUDA error";
+    case MOE_ERR_TIMEOUT:
+        return "device-side wait timed out";
+    case MOE_ERR_UNSUPPORTED:
+        return "unsupported configuration";
+    default:
+        return "unknown status";
+    }
+}
+
+size_t moe_layout_workspace_bytes(int T, int k, int E)
+{
+    if (!pairs_ok(T, k) || E < 1 || E > MOE_MAX_EXPERTS)
+        return 0;
+    return moe::layout_workspace_bytes((int64_t)T * k, E);
+}
+
+moe_status moe_layout(int T, int k, int E, int R, const int32_t *topk_idx,
+                      int32_t *expert_counts, int32_t *expert_offsets, int32_t *rank_offsets,
+                      int32_t *slot_of, int32_t *src_of, void *workspace,
+                      size_t workspace_bytes, uint32_t *err_word, cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || E < 1 || R < 1 || E % R != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (E > MOE_MAX_EXPERTS)
+        return MOE_ERR_UNSUPPORTED;
+    if (!expert_counts || !expert_offsets || !rank_offsets)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !slot_of || !src_of || !workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 4) || !aligned(expert_counts, 4) || !aligned(expert_offsets, 4) ||
+        !aligned(rank_offsets, 4) || !aligned(slot_of, 4) || !aligned(src_of, 4) ||
+        !aligned(workspace, 16) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && workspace_bytes < moe::layout_workspace_bytes((int64_t)T * k, E))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_layout(T, k, E, R, topk_idx, expert_counts, expert_offsets,
+                                        rank_offsets, slot_of, src_of, workspace, err_word,
+                                        stream));
+}
+
+moe_status moe_dispatch(int T, int H, int k, const void *x, const int32_t *slot_of, void *recv,
+                        uint32_t *err_word, cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !slot_of || !recv))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(slot_of, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_dispatch_bf16(T, H, k, x, slot_of, recv, err_word, stream));
+}
+
+moe_status moe_dispatch_quant(int T, int H, int k, const void *x, const int32_t *slot_of,
+                              uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
+                              cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 128 || H % 128 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !slot_of || !recv_q || !recv_scales))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv_q, 16) || !aligned(recv_scales, 16) ||
+        !aligned(slot_of, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_dispatch_fp8(T, H, k, x, slot_of, recv_q, recv_scales, err_word,
+                                              stream));
+}
+
+moe_status moe_combine(int T, int H, int k, const void *y, const int32_t *slot_of,
+                       const float *topk_w, void *out, int out_dtype, uint32_t *err_word,
+                       cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (out_dtype != MOE_OUT_BF16 && out_dtype != MOE_OUT_F32)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!y || !slot_of || !topk_w || !out))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(out, 16) || !aligned(slot_of, 4) || !aligned(topk_w, 4) ||
+        !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine(T, H, k, y, slot_of, topk_w, out,
+                                         out_dtype == MOE_OUT_F32, err_word, stream));
+}
+
+moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t stream, uint32_t *bits_out)
+{
+    if (!err_word || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    uint32_t bits = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaMemcpy(&bits, err_word, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (clear && bits != 0) {
+        if (cudaMemsetAsync(err_word, 0, sizeof bits, stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    if (bits_out)
+        *bits_out = bits;
+    if (bits & MOE_ERRBIT_TIMEOUT)
+        return MOE_ERR_TIMEOUT;
+    if (bits & MOE_ERRBIT_BAD_INDEX)
+        return MOE_ERR_BAD_INDEX;
+    return MOE_OK;
+}
+
+}  // extern "C"

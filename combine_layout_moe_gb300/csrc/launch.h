@@ -1,0 +1,36 @@
+// Internal launchers behind the C ABI (abi.cu).  Arguments are already
+// validated by the caller; each returns the CUDA status of its launches.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+size_t layout_workspace_bytes(int64_t N, int E);
+
+cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
+                          int32_t *expert_counts, int32_t *expert_offsets,
+                          int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
+                          void *workspace, uint32_t *err_word, cudaStream_t stream);
+
+cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32_t *slot_of,
+                                 void *recv, uint32_t *err_word, cudaStream_t stream);
+
+cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
+                                uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
+                                cudaStream_t stream);
+
+cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *slot_of,
+                           const float *topk_w, void *out, bool out_f32,
+                           uint32_t *err_word, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Grid size for a warp-per-item kernel: enough CTAs for `items` warp items,
+// capped at the number of co-resident CTAs on the whole GPU.
+int warp_item_grid(const void *kernel, int threads, size_t smem, int64_t items);
+
+}  // namespace moe

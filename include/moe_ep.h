@@ -1,0 +1,176 @@
+/*
+ * moe_ep.h -- C ABI of the GB300 MoE expert-parallel layout / dispatch / combine
+ * library (libmoe_ep.so, sm_103a kernels).
+ *
+ * Problem statement (shared by the pages): T tokens with hidden size H, each
+ * routed by a top-k router to k of E experts; the experts are spread over R
+ * expert-parallel ranks in contiguous blocks of E/R (expert e lives on rank
+ * e / (E/R)).  On one GPU the ranks are contiguous segments of one HBM buffer.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or keeps a pointer past the call.
+ *   - Every call is asynchronous and ordered on `stream`; none copies data back
+ *     to the host.  MOE_OK means the work was enqueued.
+ *   - Arguments are checked before anything is launched; a bad argument returns
+ *     MOE_ERR_INVALID_ARG and launches nothing.  Payload pointers (x, recv, y,
+ *     out, recv_q, recv_scales) must be 16-byte aligned; index/weight arrays
+ *     4-byte aligned.
+ *   - Problems found on the device (an expert id outside [0, E), a slot outside
+ *     [0, T*k)) skip the offending element and OR a bit into `*err_word` (a
+ *     device uint32 the caller zero-fills once; NULL disables reporting).
+ *     moe_read_error() synchronises the stream and reports it.  Outputs are
+ *     undefined after any error.
+ *   - A failed CUDA launch returns MOE_ERR_CUDA.
+ */
+#ifndef MOE_EP_H
+#define MOE_EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* rejected on the host, nothing launched            */
+    MOE_ERR_BAD_INDEX = 2,   /* device saw an expert id or slot out of range      */
+    MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed              */
+    MOE_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up                */
+    MOE_ERR_UNSUPPORTED = 5  /* well-formed request outside this build's limits   */
+} moe_status;
+
+typedef enum moe_out_dtype { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 } moe_out_dtype;
+
+/* bits OR-ed into *err_word by the kernels */
+#define MOE_ERRBIT_BAD_INDEX 0x1u
+#define MOE_ERRBIT_TIMEOUT 0x2u
+
+/* largest expert count the layout kernels hold in shared memory */
+#define MOE_MAX_EXPERTS 1024
+
+/* ABI revision; bumped on any signature change. */
+MOE_API int moe_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+MOE_API const char *moe_status_string(int status);
+
+/*
+ * Bytes of device workspace moe_layout needs for (T, k, E); 0 for bad sizes.
+ * The workspace holds per-tile expert counts; its contents need no
+ * initialisation and are scratch between calls.
+ */
+MOE_API size_t moe_layout_workspace_bytes(int T, int k, int E);
+
+/*
+ * moe_layout -- count, exclusive scan and stable slot map.
+ *
+ * UBEP, section 2.3 and Figure 2 (dispatch Phase 5: per-expert token counts give
+ * offsets, tokens are reordered contiguously per expert) and section 4 (receive
+ * region partitioned by source and expert); StrataCL, Appendix D (per-expert
+ * counts, prefix-sum offsets and token-local offsets are the placement metadata
+ * that dispatch and combine reuse).
+ *
+ *   topk_idx        [T, k] int32, row-major; expert id of token t's j-th choice
+ *   expert_counts   [E]    out: number of (t, j) pairs routed to expert e
+ *   expert_offsets  [E+1]  out: exclusive prefix sum of expert_counts; [E] = T*k
+ *   rank_offsets    [R+1]  out: expert_offsets[r * E/R], the start of rank r's
+ *                          segment of the receive buffer; [R] = T*k
+ *   slot_of         [T, k] out: receive-buffer row of (t, j)
+ *   src_of          [T*k]  out: inverse map, src_of[slot_of[t,j]] = t*k + j
+ *   workspace       moe_layout_workspace_bytes(T, k, E) bytes of device scratch
+ *
+ * Slot order is (rank, expert, token, j): rank-segmented, expert-contiguous,
+ * and stable in (t, j), with no padding.  The result is deterministic and
+ * does not depend on the launch configuration.  1 <= k, 1 <= E <=
+ * MOE_MAX_EXPERTS, E % R == 0, 0 <= T, T*k < 2^31.  T == 0 writes zero counts
+ * and offsets.
+ */
+MOE_API moe_status moe_layout(int T, int k, int E, int R, const int32_t *topk_idx,
+                      int32_t *expert_counts, int32_t *expert_offsets,
+                      int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
+                      void *workspace, size_t workspace_bytes, uint32_t *err_word,
+                      cudaStream_t stream);
+
+/*
+ * moe_dispatch -- bf16 token rows scattered into the packed receive buffer.
+ *
+ * UBEP, section 2.3 (Phase 2: each token is sent to every expert it chose) and
+ * section 4 (senders write directly into the partitioned receive region);
+ * RailWave, section 3.2 (payload packed without padding).
+ *
+ *   x        [T, H]   bf16 hidden states, row-major
+ *   slot_of  [T, k]   from moe_layout
+ *   recv     [T*k, H] out: recv[slot_of[t, j], :] = x[t, :]  (bit copy)
+ *
+ * H % 8 == 0 (16-byte rows).
+ */
+MOE_API moe_status moe_dispatch(int T, int H, int k, const void *x, const int32_t *slot_of,
+                        void *recv, uint32_t *err_word, cudaStream_t stream);
+
+/*
+ * moe_dispatch_quant -- dispatch with fused FP8-E4M3 block quantisation.
+ *
+ * UBEP, Table 3 (the DeepSeek-R1 / V3.2 deployments run W8A8; the pages give no
+ * further recipe).  Reading implemented: per token row, blocks of 128 channels;
+ * amax = max |x|; scale = amax / 448 and inv = 448 / amax, each rounded to
+ * nearest in fp32; code = e4m3(x * inv) rounded to nearest-even with saturation
+ * to +-448.  A block with amax == 0, or whose 448 / amax overflows fp32, stores
+ * scale 1 and signed zero codes.  Every one of a token's k slots receives the
+ * same codes and scales.
+ *
+ *   x            [T, H]      bf16
+ *   recv_q       [T*k, H]    out: E4M3 codes (one byte each)
+ *   recv_scales  [T*k, H/128] out: fp32 dequantisation scales, row-major
+ *
+ * H % 128 == 0.
+ */
+MOE_API moe_status moe_dispatch_quant(int T, int H, int k, const void *x, const int32_t *slot_of,
+                              uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
+                              cudaStream_t stream);
+
+/*
+ * moe_combine -- gather expert outputs back to token order, router-weighted.
+ *
+ * HyperParallel-MoE, section 2.2 (expert outputs are weighted by the routing
+ * scores and combined) and section 4.1 (Combine accumulates the top-k
+ * contributions according to routing scores); RailWave, section 3 (combine
+ * uses the saved dispatch metadata to return rows to their token positions).
+ *
+ *   y        [T*k, H] bf16 expert outputs in receive order
+ *   slot_of  [T, k]   from moe_layout
+ *   topk_w   [T, k]   fp32 router weights (used as given, not renormalised)
+ *   out      [T, H]   out: bf16 (out_dtype MOE_OUT_BF16) or fp32 (MOE_OUT_F32)
+ *
+ * out[t, h] = round(sum_j w[t, j] * y[slot_of[t, j], h]) with fp32 accumulation:
+ * acc = +0, then acc = fma(w[t, j], y, acc) for j = 0 .. k-1, then one rounding
+ * to the output type (nearest-even).  H % 8 == 0.
+ */
+MOE_API moe_status moe_combine(int T, int H, int k, const void *y, const int32_t *slot_of,
+                       const float *topk_w, void *out, int out_dtype, uint32_t *err_word,
+                       cudaStream_t stream);
+
+/*
+ * moe_read_error -- synchronise `stream`, read the device error word into
+ * *bits_out (may be NULL), clear it when `clear` is non-zero, and return
+ * MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_TIMEOUT (timeout wins when both bits
+ * are set).  MOE_ERR_CUDA if the synchronisation or copy fails.
+ */
+MOE_API moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t stream,
+                          uint32_t *bits_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_EP_H */

@@ -1,0 +1,98 @@
+"""The C ABI library loads without a GPU, exports every symbol include/moe_ep.h
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_ep.h")
+
+
+@pytest.fixture(scope="module")
+def m():
+    import __graft_entry__
+    __graft_entry__._cuda_build_module().build()
+    import combine_layout_moe_gb300 as pkg
+    return pkg
+
+
+def declared():
+    text = open(HEADER).read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+
+
+def test_header_declares_entry_points():
+    names = declared()
+    for n in ("moe_layout", "moe_dispatch", "moe_dispatch_quant", "moe_combine",
+              "moe_layout_workspace_bytes", "moe_read_error", "moe_status_string",
+              "moe_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(m):
+    lib = ctypes.CDLL(m.LIB_PATH)
+    for n in declared():
+        assert hasattr(lib, n), n
+        assert n in m.SIGNATURES, f"binding lacks {n}"
+
+
+def test_status_strings_and_version(m):
+    assert m.moe_abi_version() == 1
+    assert m.moe_status_string(0) == "ok"
+    assert "range" in m.moe_status_string(m.MOE_ERR_BAD_INDEX)
+    assert m.moe_status_string(99) == "unknown status"
+
+
+def test_workspace_bytes(m):
+    assert m.moe_layout_workspace_bytes(1024, 8, 256) >= 256
+    assert m.moe_layout_workspace_bytes(0, 8, 256) == 256
+    assert m.moe_layout_workspace_bytes(-1, 8, 256) == 0
+    assert m.moe_layout_workspace_bytes(1 << 28, 8, 256) == 0      # T*k >= 2^31
+    assert m.moe_layout_workspace_bytes(16, 2, 4096) == 0          # E above the maximum
+    # grows with the tile count, capped at 128 tiles x E int32
+    assert m.moe_layout_workspace_bytes(1 << 20, 8, 256) == 128 * 256 * 4
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 2, 8, 2),      # T < 0
+    (4, 0, 8, 2),       # k < 1
+    (4, 2, 6, 4),       # E % R
+    (4, 2, 8, 0),       # R < 1
+    (1 << 28, 8, 8, 2),  # T*k >= 2^31
+])
+def test_layout_rejects_bad_sizes(m, args):
+    T, k, E, R = args
+    st = m._lib.moe_layout(T, k, E, R, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None,
+                           None)
+    assert st == m.MOE_ERR_INVALID_ARG
+
+
+def test_layout_rejects_small_workspace_and_misalignment(m):
+    L = m._lib
+    assert L.moe_layout(1024, 8, 256, 32, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, None,
+                        None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_layout(4, 2, 8, 2, FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None,
+                        None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_layout(4, 2, 8, 2, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None,
+                        None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_layout(4, 2, 2048, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None,
+                        None) == m.MOE_ERR_UNSUPPORTED
+
+
+def test_payload_calls_reject_bad_shapes_and_alignment(m):
+    L = m._lib
+    bad = m.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch(4, 12, 2, FAKE, FAKE, FAKE, None, None) == bad          # H % 8
+    assert L.moe_dispatch(4, 64, 2, FAKE + 8, FAKE, FAKE, None, None) == bad      # x align
+    assert L.moe_dispatch(4, 64, 2, FAKE, FAKE, None, None, None) == bad          # null recv
+    assert L.moe_dispatch_quant(4, 192, 2, FAKE, FAKE, FAKE, FAKE, None, None) == bad
+    assert L.moe_dispatch_quant(4, 256, 2, FAKE, FAKE, FAKE, FAKE + 4, None, None) == bad
+    assert L.moe_combine(4, 64, 2, FAKE, FAKE, FAKE, FAKE, 2, None, None) == bad  # dtype
+    assert L.moe_combine(4, 64, 2, FAKE, FAKE, FAKE, FAKE + 8, 0, None, None) == bad
+    assert L.moe_combine(4, 64, 0, FAKE, FAKE, FAKE, FAKE, 0, None, None) == bad
+    assert L.moe_read_error(None, 1, None, None) == bad

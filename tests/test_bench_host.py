@@ -1,0 +1,77 @@
+"""bench.py host logic on the CPU: the max-over-ranks reduction across two gloo
+ranks, the algorithmic byte model, and the reference arm's JSON line."""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    v = bench.allreduce_max(10.0 * (rank + 1))
+    bench.barrier()
+    q.put((rank, v))
+    dist.destroy_process_group()
+
+
+def test_allreduce_max_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 20.0), (1, 20.0)]
+
+
+def test_allreduce_single_process_is_identity():
+    assert bench.allreduce_max(3.5) == 3.5
+
+
+def test_byte_model_dsv3_decode():
+    T, H, k, E, R = 1024, 7168, 8, 256, 32
+    assert bench.kernel_bytes("dispatch_bf16", T, H, k, E, R) == 2 * T * H * (1 + k) + 4 * T * k
+    assert bench.kernel_bytes("combine", T, H, k, E, R) == 2 * T * H * (1 + k) + 8 * T * k
+    # ~132 MB each; 19.5 us at 6787 GB/s
+    assert abs(bench.kernel_bytes("combine", T, H, k, E, R) / 1e6 - 132.19) < 0.01
+    fp8 = bench.kernel_bytes("dispatch_fp8", 8192, 7168, 8, 256, 32)
+    assert fp8 == 2 * 8192 * 7168 + 4 * 65536 + 65536 * 7168 + 4 * 65536 * 56
+
+
+def test_reference_arm_prints_one_json_line():
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--config", "tiny", "--steps", "3", "--warmup", "3"])
+    lines = [l for l in buf.getvalue().splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["higher_is_better"] is True
+
+
+def test_warmup_below_three_rejected():
+    with pytest.raises(SystemExit):
+        bench.main(["--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "2"])
