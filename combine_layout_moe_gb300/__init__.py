@@ -35,6 +35,7 @@ SIGNATURES = {
     "moe_dispatch_quant": ([_I, _I, _I, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_combine": ([_I, _I, _I, _P, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_read_error": ([_U32P, _I, _P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
+    "moe_layout_noalloc": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
 }
 
 
@@ -137,6 +138,21 @@ def moe_layout(topk_idx: torch.Tensor, E: int, R: int, *, workspace: Optional[to
     return out
 
 
+def moe_layout_noalloc(topk_idx: torch.Tensor, E: int, R: int, *, out: Layout,
+                       err_word: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> Layout:
+    """moe_layout for callers that cannot allocate: the outputs are passed in
+    (`out`) and the library's fixed device scratch array replaces the
+    workspace, so the call allocates nothing."""
+    T, k = topk_idx.shape
+    _want(topk_idx, "topk_idx", torch.int32)
+    _check(_lib.moe_layout_noalloc(T, k, E, R, _ptr(topk_idx), _ptr(out.expert_counts),
+                                   _ptr(out.expert_offsets), _ptr(out.rank_offsets),
+                                   _ptr(out.slot_of), _ptr(out.src_of), _ptr(err_word),
+                                   _stream(stream)), "moe_layout_noalloc")
+    return out
+
+
 def moe_dispatch(x: torch.Tensor, slot_of: torch.Tensor, *, recv: Optional[torch.Tensor] = None,
                  err_word: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
@@ -210,6 +226,6 @@ def moe_read_error(err_word: torch.Tensor, clear: bool = True,
 
 __all__ = [
     "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word",
-    "moe_layout_workspace_bytes", "moe_layout", "moe_dispatch", "moe_dispatch_quant",
+    "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
     "moe_combine", "moe_read_error", "LIB_PATH", "SIGNATURES",
 ]

@@ -161,6 +161,35 @@ MOE_API moe_status moe_combine(int T, int H, int k, const void *y, const int32_t
                        cudaStream_t stream);
 
 /*
+ * moe_layout_noalloc -- moe_layout for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a deployment convenience.
+ *
+ * Some callers cannot call cudaMalloc (or an allocator built on it) when they
+ * run the layout -- for example code handed fixed buffers by a host framework
+ * that owns all allocation, or a runtime that forbids allocation after start-
+ * up -- so they cannot supply moe_layout's workspace.  This entry point takes
+ * the same arguments minus the workspace and produces the same outputs as
+ * moe_layout; the per-tile count table lives in a fixed device array of
+ * MOE_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address; make that first call before any stream capture.  All calls
+ * on one device share the array and its contents persist between calls:
+ * calls whose work overlaps on the GPU (unordered streams) race on it.
+ * Nothing in it needs zeroing.  Requests whose count table would exceed
+ * MOE_NOALLOC_SCRATCH_BYTES (more than 512 experts with the largest token
+ * counts) return MOE_ERR_UNSUPPORTED without launching; moe_layout handles
+ * them.  The call allocates and frees nothing.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+
+MOE_API moe_status moe_layout_noalloc(int T, int k, int E, int R, const int32_t *topk_idx,
+                              int32_t *expert_counts, int32_t *expert_offsets,
+                              int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
+                              uint32_t *err_word, cudaStream_t stream);
+
+/*
  * moe_read_error -- synchronise `stream`, read the device error word into
  * *bits_out (may be NULL), clear it when `clear` is non-zero, and return
  * MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_TIMEOUT (timeout wins when both bits
