@@ -6,18 +6,26 @@
 // routing scores); RailWave, section 3 (combine uses the saved dispatch
 // metadata to return rows to their token positions).
 //
-// GPU design: a pull.  The work item is one warp on one (token, row chunk).
-// Each lane holds 8 channels x U vectors; the k source rows are loaded KC at a
-// time (KC x U independent 16-byte loads in flight per lane, 512 contiguous
-// bytes per warp instruction), then folded into fp32 accumulators with one
-// fused multiply-add per slot in slot order j = 0..k-1, starting from +0.  The
-// result is rounded once (nearest-even) and stored with 16-byte stores.  No
-// atomics: every output element is written by exactly one lane, so the result
-// is deterministic.
+// GPU design: a pull through a bulk-copy pipeline.  One persistent CTA per SM
+// owns a contiguous range of work units; a unit is one token and one chunk of
+// CH bytes of each of its k source rows (k * CH ~ 16 KB).  A producer warp
+// issues one cp.async.bulk per source row chunk into a ring of shared-memory
+// stages, completing on the stage's "full" mbarrier; consumer warps wait on it,
+// fold the k chunks into fp32 accumulators with one fused multiply-add per
+// slot in slot order j = 0..k-1 (starting from +0), round once (nearest-even),
+// store 16-byte vectors, and release the stage through its "empty" mbarrier.
+// With 12 stages the SM keeps up to ~190 KB of reads in flight without holding
+// them in registers.  Every output element is written by exactly one lane: no
+// atomics, deterministic.  Every mbarrier wait is bounded and reports
+// MOE_ERRBIT_TIMEOUT if it gives up.
+//
+// For k > 32 a register-only variant (one warp per token and row chunk, KC
+// source rows loaded at a time) does the same arithmetic in the same order.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace moe {
 
@@ -29,6 +37,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2)
                    const float *__restrict__ topk_w, void *__restrict__ out, int out_f32, int k,
                    int C, int groups, int64_t items, int N, uint32_t *err_word)
 {
+    wait_prior_grid();
+    allow_next_grid();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * (COMBINE_THREADS / 32);
     for (int64_t it = (int64_t)blockIdx.x * (COMBINE_THREADS / 32) + (threadIdx.x >> 5);
@@ -110,6 +120,187 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2)
     }
 }
 
+constexpr int CT_CONSUMERS = 6;
+constexpr int CT_THREADS = 32 * (CT_CONSUMERS + 1);
+constexpr int CT_STAGES = 12;  // a multiple of CT_CONSUMERS: consumer c owns stages c, c + 6
+constexpr int CT_STAGE_TARGET = 16384;
+constexpr int CT_BAR_BYTES = 256;  // 2 * CT_STAGES mbarriers, padded
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(CT_THREADS, 1)
+    combine_bulk_kernel(const uint8_t *__restrict__ y, const int32_t *__restrict__ slot_of,
+                        const float *__restrict__ topk_w, void *__restrict__ out, int out_f32,
+                        int T, int H, int k, int CH, int nchunks, int64_t units,
+                        uint32_t *err_word)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t bars = smem_addr(smem);
+    const uint32_t stages = bars + CT_BAR_BYTES;
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (CT_STAGES + s); };
+    const uint32_t stage_bytes = (uint32_t)k * CH;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t rowbytes = 2 * (int64_t)H;
+    const int N = T * k;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < CT_STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    wait_prior_grid();
+    allow_next_grid();
+
+    // this CTA's contiguous range of units
+    const int64_t u0 = units * blockIdx.x / gridDim.x;
+    const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
+    const int64_t nloc = u1 - u0;
+    if (nloc <= 0)
+        return;
+
+    if (warp == 0) {
+        // ---------------- producer: one bulk copy per source row chunk
+        int64_t cur_t = u0 / nchunks;
+        int32_t cur_slot = lane < k ? ld_nc_s32(slot_of + cur_t * k + lane) : 0;
+        int32_t nxt_slot = (lane < k && cur_t + 1 < T) ? ld_nc_s32(slot_of + (cur_t + 1) * k + lane) : 0;
+        int64_t n = 0;
+        bool timed_out = false;
+        for (; n < nloc; ++n) {
+            const int64_t u = u0 + n;
+            const int64_t t = u / nchunks;
+            const int c = (int)(u - t * nchunks);
+            if (t != cur_t) {
+                cur_t = t;
+                cur_slot = nxt_slot;
+                nxt_slot = (lane < k && t + 1 < T) ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+            }
+            const int s = (int)(n % CT_STAGES);
+            const uint32_t r = (uint32_t)(n / CT_STAGES);
+            if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1)) {
+                timed_out = true;
+                break;
+            }
+            const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
+            const bool ok = lane < k && (unsigned)cur_slot < (unsigned)N;
+            const unsigned okmask = __ballot_sync(FULL_MASK, ok);
+            if (lane == 0) {
+                if (c == 0 && okmask != (k >= 32 ? FULL_MASK : ((1u << k) - 1u)))
+                    report(err_word, MOE_ERRBIT_BAD_INDEX);
+                mbar_arrive_expect_tx(full(s), (uint32_t)__popc(okmask) * cb);
+            }
+            __syncwarp();
+            if (ok)
+                bulk_g2s(stages + (uint32_t)s * stage_bytes + (uint32_t)lane * CH,
+                         y + (int64_t)cur_slot * rowbytes + (int64_t)c * CH, cb, full(s));
+        }
+        if (timed_out && lane == 0)
+            report(err_word, MOE_ERRBIT_TIMEOUT);
+        // drain: every copy this CTA issued has landed before it exits
+        const int64_t first = n > CT_STAGES ? n - CT_STAGES : 0;
+        for (int64_t m = first + lane; m < n; m += 32) {
+            if (!mbar_wait(full((int)(m % CT_STAGES)), (uint32_t)(m / CT_STAGES) & 1))
+                report(err_word, MOE_ERRBIT_TIMEOUT);
+        }
+        return;
+    }
+
+    // ---------------- consumers: unit n goes to warp 1 + n % CT_CONSUMERS
+    const int cw = warp - 1;
+    for (int64_t n = cw; n < nloc; n += CT_CONSUMERS) {
+        const int64_t u = u0 + n;
+        const int64_t t = u / nchunks;
+        const int c = (int)(u - t * nchunks);
+        const int s = (int)(n % CT_STAGES);
+        const uint32_t r = (uint32_t)(n / CT_STAGES);
+        const int32_t sl = lane < k ? ld_nc_s32(slot_of + t * k + lane) : -1;
+        const float wl = lane < k ? ld_nc_f32(topk_w + t * k + lane) : 0.0f;
+        const unsigned okmask = __ballot_sync(FULL_MASK, lane < k && (unsigned)sl < (unsigned)N);
+        float w[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            w[j] = __shfl_sync(FULL_MASK, wl, j);
+        if (!mbar_wait(full(s), r & 1)) {
+            if (lane == 0)
+                report(err_word, MOE_ERRBIT_TIMEOUT);
+            return;
+        }
+        const int cb = (int)min((int64_t)CH, rowbytes - (int64_t)c * CH);
+        const uint32_t base = stages + (uint32_t)s * stage_bytes;
+        const int64_t out_elem0 = t * H + (int64_t)c * (CH / 2);
+        for (int v = lane; v < cb / 16; v += 32) {
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                acc[i] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (j < k && ((okmask >> j) & 1u)) {
+                    const uint4 q = lds128(base + (uint32_t)j * CH + (uint32_t)v * 16);
+                    const uint32_t p[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        acc[2 * h] = __fmaf_rn(w[j], bf16lo(p[h]), acc[2 * h]);
+                        acc[2 * h + 1] = __fmaf_rn(w[j], bf16hi(p[h]), acc[2 * h + 1]);
+                    }
+                }
+            }
+            const int64_t e0 = out_elem0 + (int64_t)v * 8;
+            if (out_f32) {
+                float *o = static_cast<float *>(out) + e0;
+                st_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                    __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+                st_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                        __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+            } else {
+                uint32_t rr[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
+                    rr[h] = *reinterpret_cast<const uint32_t *>(&b);
+                }
+                st_v4(static_cast<__nv_bfloat16 *>(out) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty(s));
+    }
+}
+
+template <int KMAX>
+static cudaError_t launch_combine_bulk(int T, int H, int k, const void *y, const int32_t *slot_of,
+                                       const float *topk_w, void *out, bool out_f32,
+                                       uint32_t *err_word, cudaStream_t stream)
+{
+    const int rowbytes = 2 * H;
+    int CH = (CT_STAGE_TARGET / k) / 16 * 16;
+    if (CH > rowbytes)
+        CH = rowbytes;
+    const int nchunks = (rowbytes + CH - 1) / CH;
+    const int64_t units = (int64_t)T * nchunks;
+    const size_t smem = CT_BAR_BYTES + (size_t)CT_STAGES * k * CH;
+    cudaError_t e = cudaFuncSetAttribute(combine_bulk_kernel<KMAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t g = units < sm_count() ? units : sm_count();
+    return launch_pdl(combine_bulk_kernel<KMAX>, dim3((unsigned)g), dim3(CT_THREADS), smem, stream,
+                      static_cast<const uint8_t *>(y), slot_of, topk_w, out, out_f32 ? 1 : 0, T, H,
+                      k, CH, nchunks, units, err_word);
+}
+
 template <int KC, int U>
 static cudaError_t launch_combine_t(int T, int H, int k, const void *y, const int32_t *slot_of,
                                     const float *topk_w, void *out, bool out_f32,
@@ -119,10 +310,9 @@ static cudaError_t launch_combine_t(int T, int H, int k, const void *y, const in
     const int groups = (C + 32 * U - 1) / (32 * U);
     const int64_t items = (int64_t)T * groups;
     const int grid = warp_item_grid((const void *)combine_kernel<KC, U>, COMBINE_THREADS, 0, items);
-    combine_kernel<KC, U><<<grid, COMBINE_THREADS, 0, stream>>>(
-        static_cast<const uint4 *>(y), slot_of, topk_w, out, out_f32 ? 1 : 0, k, C, groups, items,
-        T * k, err_word);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel<KC, U>, dim3(grid), dim3(COMBINE_THREADS), 0, stream,
+                      static_cast<const uint4 *>(y), slot_of, topk_w, out, out_f32 ? 1 : 0, k, C,
+                      groups, items, T * k, err_word);
 }
 
 cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *slot_of,
@@ -131,6 +321,10 @@ cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *sl
 {
     if (T == 0)
         return cudaSuccess;
+    if (k <= 8)
+        return launch_combine_bulk<8>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);
+    if (k <= 32)
+        return launch_combine_bulk<32>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);
     // KC x U ~ 16 independent 16-byte loads in flight per lane.
     if (k <= 2)
         return launch_combine_t<2, 4>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);

@@ -60,6 +60,15 @@ __device__ __forceinline__ void report(uint32_t *err_word, uint32_t bit)
         atomicOr(err_word, bit);
 }
 
+// Programmatic dependent launch.  Every kernel waits for the grid before it in
+// the stream to finish (and its writes to be visible) before its first global
+// memory access, then lets the next grid in the stream launch early: that
+// grid's CTAs become resident and park in their own wait, so the launch gap
+// between back-to-back kernels is hidden.  Both are no-ops for a kernel
+// launched without the programmatic-serialisation attribute.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // bf16 pair (packed in a 32-bit word, low half first) widened to two floats.
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

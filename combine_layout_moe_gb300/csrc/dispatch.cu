@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
                          uint4 *__restrict__ recv, int k, int C, int groups, int64_t items,
                          int N, uint32_t *err_word)
 {
+    wait_prior_grid();
+    allow_next_grid();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * (DISPATCH_THREADS / 32);
     for (int64_t it = (int64_t)blockIdx.x * (DISPATCH_THREADS / 32) + (threadIdx.x >> 5);
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
                         uint8_t *__restrict__ recv_q, float *__restrict__ recv_scales, int k,
                         int H, int groups, int64_t items, int N, uint32_t *err_word)
 {
+    wait_prior_grid();
+    allow_next_grid();
     const int lane = threadIdx.x & 31;
     const int C = H >> 3;    // 16-byte vectors per row
     const int B = H >> 7;    // 128-channel blocks per row
@@ -177,10 +181,9 @@ cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32
     const int64_t items = (int64_t)T * groups;
     const int grid = warp_item_grid((const void *)dispatch_bf16_kernel<DISPATCH_U>,
                                     DISPATCH_THREADS, 0, items);
-    dispatch_bf16_kernel<DISPATCH_U><<<grid, DISPATCH_THREADS, 0, stream>>>(
-        static_cast<const uint4 *>(x), slot_of, static_cast<uint4 *>(recv), k, C, groups, items,
-        T * k, err_word);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_bf16_kernel<DISPATCH_U>, dim3(grid), dim3(DISPATCH_THREADS), 0,
+                      stream, static_cast<const uint4 *>(x), slot_of, static_cast<uint4 *>(recv),
+                      k, C, groups, items, T * k, err_word);
 }
 
 cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
@@ -194,10 +197,9 @@ cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_
     const int64_t items = (int64_t)T * groups;
     const int grid = warp_item_grid((const void *)dispatch_fp8_kernel<QUANT_U>,
                                     DISPATCH_THREADS, 0, items);
-    dispatch_fp8_kernel<QUANT_U><<<grid, DISPATCH_THREADS, 0, stream>>>(
-        static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H, groups, items, T * k,
-        err_word);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_fp8_kernel<QUANT_U>, dim3(grid), dim3(DISPATCH_THREADS), 0,
+                      stream, static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H,
+                      groups, items, T * k, err_word);
 }
 
 }  // namespace moe

@@ -26,6 +26,26 @@ cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *sl
                            const float *topk_w, void *out, bool out_f32,
                            uint32_t *err_word, cudaStream_t stream);
 
+// Launches `kernel` on `stream` with programmatic stream serialisation, so it
+// may become resident while the previous kernel in the stream is still running
+// (the kernel itself waits for that grid before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

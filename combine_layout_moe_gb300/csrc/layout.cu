@@ -6,20 +6,23 @@
 // prefix-sum offsets and token-local offsets.
 //
 // GPU design.  The (token, slot) pairs i = t*k + j are cut into equal
-// contiguous tiles, one per CTA, and each tile into equal warp spans (UBEP
-// section 3.3's token-level load partition: loads differ by at most one warp
-// step).  Two launches, no cross-CTA waiting:
-//   count   each warp builds a private histogram of its span in shared memory
-//           (peers found with match.any, one shared-memory add per group of
-//           equal experts); the CTA writes its per-expert tile counts.
-//   assign  each CTA re-counts its tile, reads the tile-count table to get the
-//           global totals (exclusive scan -> expert offsets) and the counts of
-//           earlier tiles, turns the per-warp histograms into per-warp cursors,
-//           and walks its span again: slot = cursor[e] + rank of the lane among
-//           earlier lanes of the same step with the same expert.
-// Slots are handed out in pair order inside each warp span, spans in order
-// inside a tile, tiles in order: the result is the stable order (expert, t, j)
-// independent of scheduling.
+// contiguous tiles of ~2048 pairs, one per CTA, and each tile into equal warp
+// spans (UBEP section 3.3's token-level load partition).  Two launches, no
+// CTA ever waits on another:
+//   count   each CTA histograms its tile with shared-memory atomics and writes
+//           one row of the tile-count table.
+//   assign  each CTA histograms its tile again per warp, column-sums the
+//           tile-count table (all tiles -> totals -> exclusive scan over
+//           experts; earlier tiles -> this tile's base), turns the per-warp
+//           histograms into per-warp cursors, and walks its span in order:
+//           slot = cursor[e] + number of lower lanes of the same 32-pair step
+//           with the same expert.  That peer mask comes from a warp multisplit:
+//           one ballot per bit of the expert id (ceil(log2 E) ballots).
+// Slots are handed out in pair order within a warp span, spans in order within
+// a tile, tiles in order: the stable order (expert, t, j), independent of
+// scheduling, with no order-dependent atomics.  Both kernels use programmatic
+// dependent launch: assign becomes resident while count runs and does its own
+// histogram pass (which needs only topk_idx) before waiting for count's table.
 #include "common.cuh"
 #include "launch.h"
 
@@ -27,9 +30,10 @@ namespace moe {
 
 constexpr int LAYOUT_THREADS = 512;
 constexpr int LAYOUT_WARPS = LAYOUT_THREADS / 32;
-constexpr int LAYOUT_TARGET_TILE = 4096;  // pairs per CTA while the tile count is small
+constexpr int LAYOUT_TARGET_TILE = 2048;  // pairs per CTA while the tile count is small
 constexpr int LAYOUT_MAX_TILES = 128;     // bounds the tile-count table each CTA reads
 constexpr int LAYOUT_BATCH = 8;           // expert ids loaded ahead per lane
+constexpr int TABLE_UNROLL = 8;           // independent table loads in flight per thread
 
 // Out-of-span lanes carry NO_PAIR; pairs with an expert id outside [0, E) carry
 // BAD_PAIR (they get slot -1 and take no slot).
@@ -37,7 +41,7 @@ constexpr int NO_PAIR = -1;
 constexpr int BAD_PAIR = -2;
 
 // Loads the expert ids of up to LAYOUT_BATCH warp steps starting at pair
-// `first` (lane-strided), marking pairs past `end` as NO_PAIR.
+// `first` (lane-strided), marking pairs at or past `end` as NO_PAIR.
 __device__ __forceinline__ void load_batch(const int32_t *__restrict__ idx, int64_t first,
                                            int64_t end, int E, int lane,
                                            int (&ev)[LAYOUT_BATCH])
@@ -55,10 +59,24 @@ __device__ __forceinline__ void load_batch(const int32_t *__restrict__ idx, int6
     }
 }
 
-// Per-warp histogram of the pairs [begin, end): wcnt[e] += #pairs with expert e.
-// Returns true (on every lane) when an out-of-range expert id was seen.
-__device__ __forceinline__ bool warp_histogram(const int32_t *__restrict__ idx, int64_t begin,
-                                               int64_t end, int E, int32_t *wcnt)
+// Lanes of the warp holding the same valid expert id as this lane (this lane
+// included when e >= 0): one ballot per bit of the id.
+__device__ __forceinline__ unsigned warp_peers(int e, int nbits)
+{
+    unsigned peers = __ballot_sync(FULL_MASK, e >= 0);
+    for (int b = 0; b < nbits; ++b) {
+        const bool bit = (e >> b) & 1;
+        const unsigned m = __ballot_sync(FULL_MASK, bit);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
+
+// hist[e] += number of pairs in [begin, end) routed to e (shared-memory
+// atomics; hist may be shared by several warps).  Returns true on every lane
+// when an out-of-range expert id was seen.
+__device__ __forceinline__ bool histogram(const int32_t *__restrict__ idx, int64_t begin,
+                                          int64_t end, int E, int32_t *hist)
 {
     const int lane = threadIdx.x & 31;
     bool bad = false;
@@ -67,12 +85,9 @@ __device__ __forceinline__ bool warp_histogram(const int32_t *__restrict__ idx, 
         load_batch(idx, first, end, E, lane, ev);
 #pragma unroll
         for (int b = 0; b < LAYOUT_BATCH; ++b) {
-            const int e = ev[b];
-            bad |= (e == BAD_PAIR);
-            const unsigned peers = __match_any_sync(FULL_MASK, e);
-            if (e >= 0 && lane == __ffs(peers) - 1)
-                wcnt[e] += __popc(peers);
-            __syncwarp();
+            bad |= ev[b] == BAD_PAIR;
+            if (ev[b] >= 0)
+                atomicAdd(hist + ev[b], 1);
         }
     }
     return __any_sync(FULL_MASK, bad);
@@ -83,31 +98,27 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
                         int32_t *__restrict__ tile_counts, uint32_t *err_word)
 {
     extern __shared__ int32_t smem[];
-    int32_t *wcnt = smem;  // [LAYOUT_WARPS][E]
-    for (int i = threadIdx.x; i < LAYOUT_WARPS * E; i += LAYOUT_THREADS)
-        wcnt[i] = 0;
+    int32_t *hist = smem;  // [E]
+    for (int e = threadIdx.x; e < E; e += LAYOUT_THREADS)
+        hist[e] = 0;
+    wait_prior_grid();
+    allow_next_grid();
     __syncthreads();
 
     const int warp = threadIdx.x >> 5;
     const int64_t begin = ((int64_t)blockIdx.x * LAYOUT_WARPS + warp) * span;
     const int64_t end = min(begin + span, N);
-    const bool bad = warp_histogram(idx, begin, end, E, wcnt + warp * E);
+    const bool bad = histogram(idx, begin, end, E, hist);
     if (bad && (threadIdx.x & 31) == 0)
         report(err_word, MOE_ERRBIT_BAD_INDEX);
     __syncthreads();
-
-    for (int e = threadIdx.x; e < E; e += LAYOUT_THREADS) {
-        int32_t s = 0;
-#pragma unroll 4
-        for (int w = 0; w < LAYOUT_WARPS; ++w)
-            s += wcnt[w * E + e];
-        tile_counts[(int64_t)blockIdx.x * E + e] = s;
-    }
+    for (int e = threadIdx.x; e < E; e += LAYOUT_THREADS)
+        tile_counts[(int64_t)blockIdx.x * E + e] = hist[e];
 }
 
 __global__ void __launch_bounds__(LAYOUT_THREADS)
-    layout_assign_kernel(const int32_t *__restrict__ idx, int64_t N, int E, int R, int span,
-                         int tiles, const int32_t *__restrict__ tile_counts,
+    layout_assign_kernel(const int32_t *__restrict__ idx, int64_t N, int E, int R, int nbits,
+                         int span, int tiles, const int32_t *__restrict__ tile_counts,
                          int32_t *__restrict__ expert_counts,
                          int32_t *__restrict__ expert_offsets,
                          int32_t *__restrict__ rank_offsets, int32_t *__restrict__ slot_of,
@@ -120,26 +131,55 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
     int32_t *carry = pre + E;                 // [LAYOUT_WARPS]: scan of warp sums
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < LAYOUT_WARPS * E; i += LAYOUT_THREADS)
+    for (int i = tid; i < LAYOUT_WARPS * E + 2 * E; i += LAYOUT_THREADS)
         wcnt[i] = 0;
     __syncthreads();
 
+    // The per-warp histogram reads only topk_idx, which was complete before the
+    // count kernel let this grid launch (count waits for the producer of
+    // topk_idx first), so it runs before the wait for the count kernel and
+    // overlaps it.  A span of at most one batch keeps its expert ids in
+    // registers for the walk below.
     const int64_t begin = ((int64_t)blockIdx.x * LAYOUT_WARPS + warp) * span;
     const int64_t end = min(begin + span, N);
-    (void)warp_histogram(idx, begin, end, E, wcnt + warp * E);
+    const bool cached = end - begin <= 32 * LAYOUT_BATCH;
+    int ev0[LAYOUT_BATCH];
+    if (cached) {
+        load_batch(idx, begin, end, E, lane, ev0);
+#pragma unroll
+        for (int b = 0; b < LAYOUT_BATCH; ++b)
+            if (ev0[b] >= 0)
+                atomicAdd(wcnt + warp * E + ev0[b], 1);
+    } else {
+        (void)histogram(idx, begin, end, E, wcnt + warp * E);
+    }
+    wait_prior_grid();
+    allow_next_grid();
 
-    // Column sums of the tile-count table: all tiles, and tiles before this one.
-    for (int e = tid; e < E; e += LAYOUT_THREADS) {
-        int32_t before = 0, after = 0;
-        int b = 0;
-#pragma unroll 8
-        for (; b < (int)blockIdx.x; ++b)
-            before += tile_counts[(int64_t)b * E + e];
-#pragma unroll 8
-        for (; b < tiles; ++b)
-            after += tile_counts[(int64_t)b * E + e];
-        offs[e] = before + after;
-        pre[e] = before;
+    // Column sums of the tile-count table.  Thread (part, e) sums rows
+    // part, part + P, ... so all threads have loads in flight.
+    {
+        const int P = E >= LAYOUT_THREADS ? 1 : LAYOUT_THREADS / E;
+        const int part = tid / E;
+        for (int e = tid % E; part < P && e < E; e += LAYOUT_THREADS) {
+            int32_t before = 0, total = 0;
+            for (int b0 = part; b0 < tiles; b0 += P * TABLE_UNROLL) {
+                int32_t v[TABLE_UNROLL];
+#pragma unroll
+                for (int u = 0; u < TABLE_UNROLL; ++u) {
+                    const int b = b0 + u * P;
+                    v[u] = b < tiles ? tile_counts[(int64_t)b * E + e] : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < TABLE_UNROLL; ++u) {
+                    const int b = b0 + u * P;
+                    total += v[u];
+                    before += b < (int)blockIdx.x ? v[u] : 0;
+                }
+            }
+            atomicAdd(offs + e, total);
+            atomicAdd(pre + e, before);
+        }
     }
     __syncthreads();
 
@@ -213,12 +253,20 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
     const unsigned lt = lanemask_lt();
     for (int64_t first = begin; first < end; first += 32 * LAYOUT_BATCH) {
         int ev[LAYOUT_BATCH];
-        load_batch(idx, first, end, E, lane, ev);
+        if (cached) {
+#pragma unroll
+            for (int b = 0; b < LAYOUT_BATCH; ++b)
+                ev[b] = ev0[b];
+        } else {
+            load_batch(idx, first, end, E, lane, ev);
+        }
 #pragma unroll
         for (int b = 0; b < LAYOUT_BATCH; ++b) {
+            if (first + b * 32 >= end)
+                break;  // warp-uniform: the rest of the batch is past the span
             const int64_t i = first + b * 32 + lane;
             const int e = ev[b];
-            const unsigned peers = __match_any_sync(FULL_MASK, e);
+            const unsigned peers = warp_peers(e, nbits);
             if (e >= 0) {
                 const int32_t s = cur[e] + __popc(peers & lt);
                 slot_of[i] = s;
@@ -227,7 +275,7 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
                 slot_of[i] = -1;
             }
             __syncwarp();
-            if (e >= 0 && lane == __ffs(peers) - 1)
+            if (e >= 0 && (peers & lt) == 0)
                 cur[e] += __popc(peers);
             __syncwarp();
         }
@@ -258,7 +306,7 @@ static LayoutPlan layout_plan(int64_t N)
     return p;
 }
 
-static size_t count_smem(int E) { return sizeof(int32_t) * (size_t)LAYOUT_WARPS * E; }
+static size_t count_smem(int E) { return sizeof(int32_t) * (size_t)E; }
 static size_t assign_smem(int E)
 {
     return sizeof(int32_t) * ((size_t)LAYOUT_WARPS * E + 2 * (size_t)E + LAYOUT_WARPS);
@@ -288,22 +336,23 @@ cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
     }
     const LayoutPlan p = layout_plan(N);
     const size_t sc = count_smem(E), sa = assign_smem(E);
+    int nbits = 0;
+    while ((1 << nbits) < E)
+        ++nbits;
     cudaError_t e = cudaSuccess;
-    if (sc > 48 * 1024)
-        e = cudaFuncSetAttribute(layout_count_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
-    if (e == cudaSuccess && sa > 48 * 1024)
+    if (sa > 48 * 1024)
         e = cudaFuncSetAttribute(layout_assign_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
     if (e != cudaSuccess)
         return e;
     int32_t *tile_counts = static_cast<int32_t *>(workspace);
-    layout_count_kernel<<<p.tiles, LAYOUT_THREADS, sc, stream>>>(topk_idx, N, E, p.span,
-                                                                  tile_counts, err_word);
-    layout_assign_kernel<<<p.tiles, LAYOUT_THREADS, sa, stream>>>(
-        topk_idx, N, E, R, p.span, p.tiles, tile_counts, expert_counts, expert_offsets,
-        rank_offsets, slot_of, src_of);
-    return cudaGetLastError();
+    e = launch_pdl(layout_count_kernel, dim3(p.tiles), dim3(LAYOUT_THREADS), sc, stream,
+                   topk_idx, N, E, p.span, tile_counts, err_word);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(layout_assign_kernel, dim3(p.tiles), dim3(LAYOUT_THREADS), sa, stream,
+                      topk_idx, N, E, R, nbits, p.span, p.tiles, tile_counts, expert_counts,
+                      expert_offsets, rank_offsets, slot_of, src_of);
 }
 
 }  // namespace moe
