@@ -37,14 +37,18 @@ def _headers():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = LIB,
+          obj_dir: str = OUT_DIR) -> str:
+    """Compile and link; `extra_flags`, `lib_path` and `obj_dir` let a tuning
+    sweep build variants (e.g. -DMOE_CT_STAGES=8) beside the shipped library."""
+    OUT = obj_dir
+    os.makedirs(OUT, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     newest_header = max((os.path.getmtime(h) for h in _headers()), default=0.0)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
         if (not force and os.path.exists(obj)
                 and os.path.getmtime(obj) >= max(os.path.getmtime(src), newest_header)):
             return obj, False
@@ -60,14 +64,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         results = list(ex.map(compile_one, sources))
     objs = [o for o, _ in results]
     rebuilt = any(c for _, c in results)
-    if force or rebuilt or not os.path.exists(LIB):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or rebuilt or not os.path.exists(lib_path):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

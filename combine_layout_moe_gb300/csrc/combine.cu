@@ -8,15 +8,16 @@
 //
 // GPU design: a pull through a bulk-copy pipeline.  One persistent CTA per SM
 // owns a contiguous range of work units; a unit is one token and one chunk of
-// CH bytes of each of its k source rows (k * CH ~ 16 KB).  A producer warp
-// issues one cp.async.bulk per source row chunk into a ring of shared-memory
-// stages, completing on the stage's "full" mbarrier; consumer warps wait on it,
-// fold the k chunks into fp32 accumulators with one fused multiply-add per
-// slot in slot order j = 0..k-1 (starting from +0), round once (nearest-even),
-// store 16-byte vectors, and release the stage through its "empty" mbarrier.
-// With 12 stages the SM keeps up to ~190 KB of reads in flight without holding
-// them in registers.  Every output element is written by exactly one lane: no
-// atomics, deterministic.  Every mbarrier wait is bounded and reports
+// CH bytes of each of its k source rows (k * CH ~ 32 KB, equal chunks).  A
+// producer warp issues one cp.async.bulk per source row chunk into a ring of 6
+// shared-memory stages, completing on the stage's "full" mbarrier, and writes
+// the token's weights and valid-slot mask into the stage header; consumer
+// warps wait on it, fold the k chunks into fp32 accumulators with one fused
+// multiply-add per slot in slot order j = 0..k-1 (starting from +0), round
+// once (nearest-even), store 16-byte vectors, and release the stage through
+// its "empty" mbarrier.  The SM keeps up to ~190 KB of reads in flight without
+// holding them in registers.  Every output element is written by exactly one
+// lane: no atomics, deterministic.  Every mbarrier wait is bounded and reports
 // MOE_ERRBIT_TIMEOUT if it gives up.
 //
 // For k > 32 a register-only variant (one warp per token and row chunk, KC
@@ -120,11 +121,25 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2)
     }
 }
 
-constexpr int CT_CONSUMERS = 6;
+// Tunables (compile-time; the defaults are the shipped configuration).
+#ifndef MOE_CT_CONSUMERS
+#define MOE_CT_CONSUMERS 6
+#endif
+#ifndef MOE_CT_STAGES
+#define MOE_CT_STAGES 6
+#endif
+#ifndef MOE_CT_STAGE_TARGET
+#define MOE_CT_STAGE_TARGET 32768
+#endif
+constexpr int CT_CONSUMERS = MOE_CT_CONSUMERS;
 constexpr int CT_THREADS = 32 * (CT_CONSUMERS + 1);
-constexpr int CT_STAGES = 12;  // a multiple of CT_CONSUMERS: consumer c owns stages c, c + 6
-constexpr int CT_STAGE_TARGET = 16384;
-constexpr int CT_BAR_BYTES = 256;  // 2 * CT_STAGES mbarriers, padded
+constexpr int CT_STAGES = MOE_CT_STAGES;
+constexpr int CT_STAGE_TARGET = MOE_CT_STAGE_TARGET;  // bytes of k row chunks per stage
+constexpr int CT_HDR_WORDS = 36;  // per stage: 32 weights, valid-slot mask, padding
+constexpr int CT_BAR_BYTES = 16 * CT_STAGES;
+constexpr int CT_HDR_BYTES = 4 * CT_HDR_WORDS * CT_STAGES;
+constexpr int CT_PREFIX = (CT_BAR_BYTES + CT_HDR_BYTES + 127) / 128 * 128;
+static_assert(CT_STAGES % CT_CONSUMERS == 0, "each consumer warp owns whole stages");
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
@@ -133,6 +148,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
     return v;
+}
+
+// Advances a (token, chunk) cursor by `step` units.
+__device__ __forceinline__ void advance(int64_t &t, int &c, int step, int nchunks)
+{
+    c += step;
+    while (c >= nchunks) {
+        c -= nchunks;
+        ++t;
+    }
 }
 
 template <int KMAX>
@@ -144,7 +169,8 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t bars = smem_addr(smem);
-    const uint32_t stages = bars + CT_BAR_BYTES;
+    float *hdr = reinterpret_cast<float *>(smem + CT_BAR_BYTES);  // [CT_STAGES][CT_HDR_WORDS]
+    const uint32_t stages = bars + CT_PREFIX;
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (CT_STAGES + s); };
     const uint32_t stage_bytes = (uint32_t)k * CH;
@@ -163,7 +189,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
     wait_prior_grid();
     allow_next_grid();
 
-    // this CTA's contiguous range of units
+    // this CTA's contiguous range of units (unit = token t, chunk c)
     const int64_t u0 = units * blockIdx.x / gridDim.x;
     const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
     const int64_t nloc = u1 - u0;
@@ -171,20 +197,28 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         return;
 
     if (warp == 0) {
-        // ---------------- producer: one bulk copy per source row chunk
-        int64_t cur_t = u0 / nchunks;
-        int32_t cur_slot = lane < k ? ld_nc_s32(slot_of + cur_t * k + lane) : 0;
-        int32_t nxt_slot = (lane < k && cur_t + 1 < T) ? ld_nc_s32(slot_of + (cur_t + 1) * k + lane) : 0;
+        // ---------------- producer: header + one bulk copy per source row chunk
+        int64_t t = u0 / nchunks;
+        int c = (int)(u0 - t * nchunks);
+        const bool kl = lane < k;
+        int32_t cur_slot = kl ? ld_nc_s32(slot_of + t * k + lane) : 0;
+        float cur_w = kl ? ld_nc_f32(topk_w + t * k + lane) : 0.0f;
+        const bool has_next = t + 1 < T;
+        int32_t nxt_slot = kl && has_next ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+        float nxt_w = kl && has_next ? ld_nc_f32(topk_w + (t + 1) * k + lane) : 0.0f;
         int64_t n = 0;
         bool timed_out = false;
         for (; n < nloc; ++n) {
-            const int64_t u = u0 + n;
-            const int64_t t = u / nchunks;
-            const int c = (int)(u - t * nchunks);
-            if (t != cur_t) {
-                cur_t = t;
-                cur_slot = nxt_slot;
-                nxt_slot = (lane < k && t + 1 < T) ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+            if (n > 0) {
+                const int64_t t_prev = t;
+                advance(t, c, 1, nchunks);
+                if (t != t_prev) {
+                    cur_slot = nxt_slot;
+                    cur_w = nxt_w;
+                    const bool more = kl && t + 1 < T;
+                    nxt_slot = more ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+                    nxt_w = more ? ld_nc_f32(topk_w + (t + 1) * k + lane) : 0.0f;
+                }
             }
             const int s = (int)(n % CT_STAGES);
             const uint32_t r = (uint32_t)(n / CT_STAGES);
@@ -193,9 +227,17 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                 break;
             }
             const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
-            const bool ok = lane < k && (unsigned)cur_slot < (unsigned)N;
+            const bool ok = kl && (unsigned)cur_slot < (unsigned)N;
             const unsigned okmask = __ballot_sync(FULL_MASK, ok);
+            float *h = hdr + s * CT_HDR_WORDS;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                const float wj = __shfl_sync(FULL_MASK, cur_w, j);
+                if (lane == 0 && j < k)
+                    h[j] = wj;
+            }
             if (lane == 0) {
+                reinterpret_cast<uint32_t *>(h)[32] = okmask;
                 if (c == 0 && okmask != (k >= 32 ? FULL_MASK : ((1u << k) - 1u)))
                     report(err_word, MOE_ERRBIT_BAD_INDEX);
                 mbar_arrive_expect_tx(full(s), (uint32_t)__popc(okmask) * cb);
@@ -218,24 +260,24 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
 
     // ---------------- consumers: unit n goes to warp 1 + n % CT_CONSUMERS
     const int cw = warp - 1;
+    int64_t t = (u0 + cw) / nchunks;
+    int c = (int)(u0 + cw - t * nchunks);
     for (int64_t n = cw; n < nloc; n += CT_CONSUMERS) {
-        const int64_t u = u0 + n;
-        const int64_t t = u / nchunks;
-        const int c = (int)(u - t * nchunks);
+        if (n > cw)
+            advance(t, c, CT_CONSUMERS, nchunks);
         const int s = (int)(n % CT_STAGES);
         const uint32_t r = (uint32_t)(n / CT_STAGES);
-        const int32_t sl = lane < k ? ld_nc_s32(slot_of + t * k + lane) : -1;
-        const float wl = lane < k ? ld_nc_f32(topk_w + t * k + lane) : 0.0f;
-        const unsigned okmask = __ballot_sync(FULL_MASK, lane < k && (unsigned)sl < (unsigned)N);
-        float w[KMAX];
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j)
-            w[j] = __shfl_sync(FULL_MASK, wl, j);
         if (!mbar_wait(full(s), r & 1)) {
             if (lane == 0)
                 report(err_word, MOE_ERRBIT_TIMEOUT);
             return;
         }
+        const float *h = hdr + s * CT_HDR_WORDS;
+        const unsigned okmask = reinterpret_cast<const uint32_t *>(h)[32];
+        float w[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            w[j] = j < k ? h[j] : 0.0f;
         const int cb = (int)min((int64_t)CH, rowbytes - (int64_t)c * CH);
         const uint32_t base = stages + (uint32_t)s * stage_bytes;
         const int64_t out_elem0 = t * H + (int64_t)c * (CH / 2);
@@ -250,9 +292,9 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                     const uint4 q = lds128(base + (uint32_t)j * CH + (uint32_t)v * 16);
                     const uint32_t p[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        acc[2 * h] = __fmaf_rn(w[j], bf16lo(p[h]), acc[2 * h]);
-                        acc[2 * h + 1] = __fmaf_rn(w[j], bf16hi(p[h]), acc[2 * h + 1]);
+                    for (int hh = 0; hh < 4; ++hh) {
+                        acc[2 * hh] = __fmaf_rn(w[j], bf16lo(p[hh]), acc[2 * hh]);
+                        acc[2 * hh + 1] = __fmaf_rn(w[j], bf16hi(p[hh]), acc[2 * hh + 1]);
                     }
                 }
             }
@@ -266,9 +308,9 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
             } else {
                 uint32_t rr[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
-                    rr[h] = *reinterpret_cast<const uint32_t *>(&b);
+                for (int hh = 0; hh < 4; ++hh) {
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * hh], acc[2 * hh + 1]);
+                    rr[hh] = *reinterpret_cast<const uint32_t *>(&b);
                 }
                 st_v4(static_cast<__nv_bfloat16 *>(out) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
             }
@@ -284,18 +326,30 @@ static cudaError_t launch_combine_bulk(int T, int H, int k, const void *y, const
                                        const float *topk_w, void *out, bool out_f32,
                                        uint32_t *err_word, cudaStream_t stream)
 {
+    // Equal chunks (multiples of 16 bytes) of about CT_STAGE_TARGET / k bytes:
+    // the fewest chunks per row whose k-row stage fits the target.
     const int rowbytes = 2 * H;
-    int CH = (CT_STAGE_TARGET / k) / 16 * 16;
-    if (CH > rowbytes)
-        CH = rowbytes;
-    const int nchunks = (rowbytes + CH - 1) / CH;
+    const int vec = rowbytes / 16;
+    int nchunks = (int)(((int64_t)rowbytes * k + CT_STAGE_TARGET - 1) / CT_STAGE_TARGET);
+    if (nchunks < 1)
+        nchunks = 1;
+    if (nchunks > vec)
+        nchunks = vec;
+    const int CH = (vec + nchunks - 1) / nchunks * 16;
+    nchunks = (rowbytes + CH - 1) / CH;
     const int64_t units = (int64_t)T * nchunks;
-    const size_t smem = CT_BAR_BYTES + (size_t)CT_STAGES * k * CH;
+    const size_t smem = CT_PREFIX + (size_t)CT_STAGES * k * CH;
     cudaError_t e = cudaFuncSetAttribute(combine_bulk_kernel<KMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    const int64_t g = units < sm_count() ? units : sm_count();
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_bulk_kernel<KMAX>, CT_THREADS,
+                                                      smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t g = units < cap ? units : cap;
     return launch_pdl(combine_bulk_kernel<KMAX>, dim3((unsigned)g), dim3(CT_THREADS), smem, stream,
                       static_cast<const uint8_t *>(y), slot_of, topk_w, out, out_f32 ? 1 : 0, T, H,
                       k, CH, nchunks, units, err_word);

@@ -18,8 +18,120 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace moe {
+
+#ifndef MOE_DB_STAGES
+#define MOE_DB_STAGES 4
+#endif
+#ifndef MOE_DB_CHUNK
+#define MOE_DB_CHUNK 8192
+#endif
+constexpr int DB_STAGES = MOE_DB_STAGES;  // row chunks in flight per pipe
+constexpr int DB_CHUNK = MOE_DB_CHUNK;    // bytes per bulk copy (last chunk of a row may be shorter)
+static_assert(DB_STAGES >= 2 && DB_STAGES <= 16, "stage ring size");
+
+// bf16 dispatch through bulk copies.  Each CTA is one warp driving one
+// pipeline over a contiguous range of units (unit = token t, chunk c of its
+// row): lane 0 loads the chunk into a ring of shared-memory stages with one
+// cp.async.bulk (completion on the stage's mbarrier); once it has landed,
+// lanes 0..k-1 each store it to their destination row with one shared ->
+// global cp.async.bulk.  A stage is refilled only after every lane's stores
+// from it have finished reading shared memory (bulk async-group accounting:
+// every lane commits one group per unit, possibly empty).  The row is read
+// from HBM once and written k times with no per-element instructions.
+__global__ void __launch_bounds__(32)
+    dispatch_bulk_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ slot_of,
+                         uint8_t *__restrict__ recv, int T, int k, int64_t rowbytes, int CH,
+                         int nchunks, int64_t units, uint32_t *err_word)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t bars = smem_addr(smem);
+    const uint32_t stages = bars + 128;
+    auto full = [&](int s) { return bars + 8u * s; };
+    const int lane = threadIdx.x;
+    const int N = T * k;
+
+    if (lane == 0) {
+        for (int s = 0; s < DB_STAGES; ++s)
+            mbar_init(full(s), 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+    wait_prior_grid();
+    allow_next_grid();
+
+    const int64_t u0 = units * blockIdx.x / gridDim.x;
+    const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
+    const int64_t nloc = u1 - u0;
+    if (nloc <= 0)
+        return;
+
+    // load cursor (lane 0 issues loads in unit order)
+    int64_t lt = u0 / nchunks;
+    int lc = (int)(u0 - lt * nchunks);
+    int64_t loaded = 0;
+    auto issue_load = [&]() {
+        const int s = (int)(loaded % DB_STAGES);
+        const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)lc * CH);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(full(s), cb);
+            bulk_g2s(stages + (uint32_t)s * CH, x + lt * rowbytes + (int64_t)lc * CH, cb, full(s));
+        }
+        ++loaded;
+        if (++lc == nchunks) {
+            lc = 0;
+            ++lt;
+        }
+    };
+    while (loaded < nloc && loaded < DB_STAGES)
+        issue_load();
+
+    // store cursor
+    int64_t t = u0 / nchunks;
+    int c = (int)(u0 - t * nchunks);
+    const bool kl = lane < k;
+    int32_t cur = kl ? ld_nc_s32(slot_of + t * k + lane) : 0;
+    int32_t nxt = kl && t + 1 < T ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+    int64_t n = 0;
+    bool timed_out = false;
+    for (; n < nloc; ++n) {
+        if (n > 0 && ++c == nchunks) {
+            c = 0;
+            ++t;
+            cur = nxt;
+            nxt = kl && t + 1 < T ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+        }
+        const int s = (int)(n % DB_STAGES);
+        if (!mbar_wait(full(s), (uint32_t)(n / DB_STAGES) & 1)) {
+            timed_out = true;
+            break;
+        }
+        const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
+        fence_proxy_async_smem();
+        if (kl) {
+            if ((unsigned)cur < (unsigned)N)
+                bulk_s2g(recv + (int64_t)cur * rowbytes + (int64_t)c * CH, stages + (uint32_t)s * CH, cb);
+            else if (c == 0)
+                report(err_word, MOE_ERRBIT_BAD_INDEX);
+        }
+        bulk_commit();
+        // refill the stage unit n-1 used with the next unit to load
+        if (n >= 1 && loaded < nloc) {
+            bulk_wait_read<1>();
+            __syncwarp();
+            issue_load();
+        }
+    }
+    if (timed_out) {
+        if (lane == 0)
+            report(err_word, MOE_ERRBIT_TIMEOUT);
+        for (int64_t m = n + lane; m < loaded; m += 32)  // let issued loads land
+            (void)mbar_wait(full((int)(m % DB_STAGES)), (uint32_t)(m / DB_STAGES) & 1);
+    }
+    bulk_wait_all();
+}
 
 constexpr int DISPATCH_THREADS = 256;
 constexpr int DISPATCH_U = 4;  // 16-byte vectors per lane per item
@@ -176,6 +288,29 @@ cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32
 {
     if (T == 0)
         return cudaSuccess;
+    if (k <= 32) {
+        const int64_t rowbytes = 2 * (int64_t)H;
+        const int CH = rowbytes < DB_CHUNK ? (int)rowbytes : DB_CHUNK;
+        const int nchunks = (int)((rowbytes + CH - 1) / CH);
+        const int64_t units = (int64_t)T * nchunks;
+        const size_t smem = 128 + (size_t)DB_STAGES * CH;
+        cudaError_t e = cudaSuccess;
+        if (smem > 48 * 1024)
+            e = cudaFuncSetAttribute(dispatch_bulk_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        int per_sm = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bulk_kernel, 32, smem) !=
+                cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        const int64_t cap = (int64_t)sm_count() * per_sm;
+        const int64_t g = units < cap ? units : cap;
+        return launch_pdl(dispatch_bulk_kernel, dim3((unsigned)g), dim3(32), smem, stream,
+                          static_cast<const uint8_t *>(x), slot_of, static_cast<uint8_t *>(recv), T,
+                          k, rowbytes, CH, nchunks, units, err_word);
+    }
     const int C = H / 8;
     const int groups = (C + 32 * DISPATCH_U - 1) / (32 * DISPATCH_U);
     const int64_t items = (int64_t)T * groups;

@@ -7,9 +7,16 @@
 
 namespace moe {
 
-// try_wait may park the thread for a hardware-chosen interval per attempt, so
-// this bounds a wait to well under a minute even in the worst case.
-constexpr uint32_t MBAR_TRY_LIMIT = 1u << 22;
+// A wait gives up after this much wall-clock time (the device's global
+// nanosecond timer), whatever the hardware does inside each try_wait.
+constexpr uint64_t MBAR_TIMEOUT_NS = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
@@ -51,14 +58,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
-// Waits until the phase with the given parity has completed; false if the
-// attempt limit ran out first.
+// Waits until the phase with the given parity has completed; false once
+// MBAR_TIMEOUT_NS has passed.  The caller must never be two or more phases
+// ahead of the barrier (parity alone cannot tell those apart): every pipeline
+// here gives each stage a single consumer that waits on its phases in order.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
-    for (uint32_t i = 0; i < MBAR_TRY_LIMIT; ++i)
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
         if (mbar_try_wait(bar, parity))
             return true;
-    return false;
+        if (global_ns() - t0 > MBAR_TIMEOUT_NS)
+            return false;
+    }
 }
 
 // Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
@@ -79,6 +93,13 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
                  "r"(bytes)
                  : "memory");
+}
+
+// Orders this thread's earlier shared-memory accesses (and what it observed
+// through mbarriers) before its later bulk-copy accesses to shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
