@@ -104,6 +104,12 @@ def moe_layout_workspace_bytes(T: int, k: int, E: int) -> int:
     return int(_lib.moe_layout_workspace_bytes(T, k, E))
 
 
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A layout workspace: zero-filled once, as moe_layout requires; reusable
+    for every later call whose moe_layout_workspace_bytes fits in it."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
 class Layout(NamedTuple):
     expert_counts: torch.Tensor   # int32 [E]
     expert_offsets: torch.Tensor  # int32 [E+1]
@@ -129,7 +135,7 @@ def moe_layout(topk_idx: torch.Tensor, E: int, R: int, *, workspace: Optional[to
                      torch.empty(T * k, dtype=torch.int32, device=dev))
     need = moe_layout_workspace_bytes(T, k, E)
     if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        workspace = new_workspace(need, dev)
     _check(_lib.moe_layout(T, k, E, R, _ptr(topk_idx), _ptr(out.expert_counts),
                            _ptr(out.expert_offsets), _ptr(out.rank_offsets), _ptr(out.slot_of),
                            _ptr(out.src_of), _ptr(workspace), workspace.numel() *
@@ -225,7 +231,7 @@ def moe_read_error(err_word: torch.Tensor, clear: bool = True,
 
 
 __all__ = [
-    "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word",
+    "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word", "new_workspace",
     "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
     "moe_combine", "moe_read_error", "LIB_PATH", "SIGNATURES",
 ]

@@ -5,26 +5,26 @@
 // Appendix D: the placement metadata is destination expert, per-expert counts,
 // prefix-sum offsets and token-local offsets.
 //
-// GPU design.  The (token, slot) pairs i = t*k + j are cut into equal
-// contiguous tiles of ~2048 pairs, one per CTA, and each tile into equal warp
-// spans (UBEP section 3.3's token-level load partition).  Two launches, no
-// CTA ever waits on another:
-//   count   each CTA histograms its tile with shared-memory atomics and writes
-//           one row of the tile-count table.
-//   assign  each CTA histograms its tile again per warp, column-sums the
-//           tile-count table (all tiles -> totals -> exclusive scan over
-//           experts; earlier tiles -> this tile's base), turns the per-warp
-//           histograms into per-warp cursors, and walks its span in order:
-//           slot = cursor[e] + number of lower lanes of the same 32-pair step
-//           with the same expert.  That peer mask comes from a warp multisplit:
-//           one ballot per bit of the expert id (ceil(log2 E) ballots).
+// GPU design: one cooperative launch, one CTA per tile.  The (token, slot)
+// pairs i = t*k + j are cut into equal contiguous tiles of ~2048 pairs (at
+// most LAYOUT_MAX_TILES tiles), and each tile into equal warp spans (UBEP
+// section 3.3's token-level load partition).
+//   1. Each warp histograms its span into a private shared-memory row (the
+//      expert ids stay in registers); the CTA writes the row sums to its row of
+//      the tile-count table.
+//   2. Grid barrier (arrival count and generation in the workspace; bounded).
+//   3. Each CTA column-sums the table (all tiles -> totals -> exclusive scan
+//      over experts; earlier tiles -> this tile's base), turns the per-warp
+//      histograms into per-warp cursors, and walks its span in order:
+//      slot = cursor[e] + number of lower lanes of the same 32-pair step with
+//      the same expert.  That peer mask comes from a warp multisplit: one
+//      ballot per bit of the expert id (ceil(log2 E) ballots).
 // Slots are handed out in pair order within a warp span, spans in order within
 // a tile, tiles in order: the stable order (expert, t, j), independent of
-// scheduling, with no order-dependent atomics.  Both kernels use programmatic
-// dependent launch: assign becomes resident while count runs and does its own
-// histogram pass (which needs only topk_idx) before waiting for count's table.
+// scheduling, with no order-dependent atomics.
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace moe {
 
@@ -34,6 +34,7 @@ constexpr int LAYOUT_TARGET_TILE = 2048;  // pairs per CTA while the tile count 
 constexpr int LAYOUT_MAX_TILES = 128;     // bounds the tile-count table each CTA reads
 constexpr int LAYOUT_BATCH = 8;           // expert ids loaded ahead per lane
 constexpr int TABLE_UNROLL = 8;           // independent table loads in flight per thread
+constexpr size_t LAYOUT_BARRIER_BYTES = 256;  // workspace head: grid-barrier count and generation
 
 // Out-of-span lanes carry NO_PAIR; pairs with an expert id outside [0, E) carry
 // BAD_PAIR (they get slot -1 and take no slot).
@@ -60,11 +61,13 @@ __device__ __forceinline__ void load_batch(const int32_t *__restrict__ idx, int6
 }
 
 // Lanes of the warp holding the same valid expert id as this lane (this lane
-// included when e >= 0): one ballot per bit of the id.
-__device__ __forceinline__ unsigned warp_peers(int e, int nbits)
+// included when e >= 0): one ballot per bit of the id (NBITS = ceil(log2 E)).
+template <int NBITS>
+__device__ __forceinline__ unsigned warp_peers(int e)
 {
     unsigned peers = __ballot_sync(FULL_MASK, e >= 0);
-    for (int b = 0; b < nbits; ++b) {
+#pragma unroll
+    for (int b = 0; b < NBITS; ++b) {
         const bool bit = (e >> b) & 1;
         const unsigned m = __ballot_sync(FULL_MASK, bit);
         peers &= bit ? m : ~m;
@@ -72,57 +75,77 @@ __device__ __forceinline__ unsigned warp_peers(int e, int nbits)
     return peers;
 }
 
-// hist[e] += number of pairs in [begin, end) routed to e (shared-memory
-// atomics; hist may be shared by several warps).  Returns true on every lane
-// when an out-of-range expert id was seen.
-__device__ __forceinline__ bool histogram(const int32_t *__restrict__ idx, int64_t begin,
-                                          int64_t end, int E, int32_t *hist)
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
 {
-    const int lane = threadIdx.x & 31;
-    bool bad = false;
-    for (int64_t first = begin; first < end; first += 32 * LAYOUT_BATCH) {
-        int ev[LAYOUT_BATCH];
-        load_batch(idx, first, end, E, lane, ev);
-#pragma unroll
-        for (int b = 0; b < LAYOUT_BATCH; ++b) {
-            bad |= ev[b] == BAD_PAIR;
-            if (ev[b] >= 0)
-                atomicAdd(hist + ev[b], 1);
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned atom_add_release_u32(unsigned *p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Sense-reversing barrier across the co-resident CTAs of a cooperative launch.
+// bar[0] counts arrivals and must be zero when a launch starts; bar[1] is the
+// generation.  Arrival is a release (it publishes what this CTA wrote before
+// its __syncthreads) and the wait an acquire.  The last CTA to arrive resets
+// the count and bumps the generation, so every launch leaves the count at zero
+// again.  The wait gives up after MBAR_TIMEOUT_NS and reports
+// MOE_ERRBIT_TIMEOUT.  Returns whether the barrier completed.
+__device__ bool grid_barrier(unsigned *bar, uint32_t *err_word)
+{
+    __shared__ int ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned *count = bar, *gen = bar + 1;
+        const unsigned g = ld_acquire_u32(gen);  // before arriving: cannot have moved yet
+        int done = 1;
+        if (atom_add_release_u32(count, 1u) == gridDim.x - 1) {
+            atomicExch(count, 0u);
+            atom_add_release_u32(gen, 1u);
+        } else {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_u32(gen) == g) {
+                if (global_ns() - t0 > MBAR_TIMEOUT_NS) {
+                    done = 0;
+                    report(err_word, MOE_ERRBIT_TIMEOUT);
+                    break;
+                }
+            }
         }
+        ok = done;
     }
-    return __any_sync(FULL_MASK, bad);
+    __syncthreads();
+    return ok != 0;
 }
 
-__global__ void __launch_bounds__(LAYOUT_THREADS)
-    layout_count_kernel(const int32_t *__restrict__ idx, int64_t N, int E, int span,
-                        int32_t *__restrict__ tile_counts, uint32_t *err_word)
-{
-    extern __shared__ int32_t smem[];
-    int32_t *hist = smem;  // [E]
-    for (int e = threadIdx.x; e < E; e += LAYOUT_THREADS)
-        hist[e] = 0;
-    wait_prior_grid();
-    allow_next_grid();
-    __syncthreads();
+// Phase timestamps for tuning builds (-DMOE_TRACE): CTA 0 stores %globaltimer
+// at each phase boundary into the 64-bit words that follow the error word.
+#ifdef MOE_TRACE
+#define LAYOUT_TRACE(n)                                                                \
+    do {                                                                               \
+        __syncthreads();                                                               \
+        if (blockIdx.x == 0 && threadIdx.x == 0 && err_word)                            \
+            reinterpret_cast<unsigned long long *>(err_word)[8 + (n)] = global_ns();   \
+    } while (0)
+#else
+#define LAYOUT_TRACE(n) \
+    do {                \
+    } while (0)
+#endif
 
-    const int warp = threadIdx.x >> 5;
-    const int64_t begin = ((int64_t)blockIdx.x * LAYOUT_WARPS + warp) * span;
-    const int64_t end = min(begin + span, N);
-    const bool bad = histogram(idx, begin, end, E, hist);
-    if (bad && (threadIdx.x & 31) == 0)
-        report(err_word, MOE_ERRBIT_BAD_INDEX);
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += LAYOUT_THREADS)
-        tile_counts[(int64_t)blockIdx.x * E + e] = hist[e];
-}
-
+template <int NBITS>
 __global__ void __launch_bounds__(LAYOUT_THREADS)
-    layout_assign_kernel(const int32_t *__restrict__ idx, int64_t N, int E, int R, int nbits,
-                         int span, int tiles, const int32_t *__restrict__ tile_counts,
-                         int32_t *__restrict__ expert_counts,
-                         int32_t *__restrict__ expert_offsets,
-                         int32_t *__restrict__ rank_offsets, int32_t *__restrict__ slot_of,
-                         int32_t *__restrict__ src_of)
+    layout_kernel(const int32_t *__restrict__ idx, int64_t N, int E, int R, int span,
+                  int tiles, unsigned *barrier, int32_t *tile_counts,
+                  int32_t *__restrict__ expert_counts, int32_t *__restrict__ expert_offsets,
+                  int32_t *__restrict__ rank_offsets, int32_t *__restrict__ slot_of,
+                  int32_t *__restrict__ src_of, uint32_t *err_word)
 {
     extern __shared__ int32_t smem[];
     int32_t *wcnt = smem;                     // [LAYOUT_WARPS][E]: counts, then cursors
@@ -133,31 +156,51 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < LAYOUT_WARPS * E + 2 * E; i += LAYOUT_THREADS)
         wcnt[i] = 0;
+    wait_prior_grid();
+    allow_next_grid();
     __syncthreads();
+    LAYOUT_TRACE(0);
 
-    // The per-warp histogram reads only topk_idx, which was complete before the
-    // count kernel let this grid launch (count waits for the producer of
-    // topk_idx first), so it runs before the wait for the count kernel and
-    // overlaps it.  A span of at most one batch keeps its expert ids in
-    // registers for the walk below.
+    // 1. per-warp histograms of this tile; the ids of a span of at most one
+    //    batch stay in registers for the walk
     const int64_t begin = ((int64_t)blockIdx.x * LAYOUT_WARPS + warp) * span;
     const int64_t end = min(begin + span, N);
     const bool cached = end - begin <= 32 * LAYOUT_BATCH;
     int ev0[LAYOUT_BATCH];
-    if (cached) {
-        load_batch(idx, begin, end, E, lane, ev0);
 #pragma unroll
-        for (int b = 0; b < LAYOUT_BATCH; ++b)
-            if (ev0[b] >= 0)
-                atomicAdd(wcnt + warp * E + ev0[b], 1);
-    } else {
-        (void)histogram(idx, begin, end, E, wcnt + warp * E);
+    for (int b = 0; b < LAYOUT_BATCH; ++b)
+        ev0[b] = NO_PAIR;
+    bool bad = false;
+    for (int64_t first = begin; first < end; first += 32 * LAYOUT_BATCH) {
+        int ev[LAYOUT_BATCH];
+        load_batch(idx, first, end, E, lane, ev);
+#pragma unroll
+        for (int b = 0; b < LAYOUT_BATCH; ++b) {
+            bad |= ev[b] == BAD_PAIR;
+            if (ev[b] >= 0)
+                atomicAdd(wcnt + warp * E + ev[b], 1);
+            ev0[b] = ev[b];
+        }
     }
-    wait_prior_grid();
-    allow_next_grid();
+    if (__any_sync(FULL_MASK, bad) && lane == 0)
+        report(err_word, MOE_ERRBIT_BAD_INDEX);
+    __syncthreads();
+    LAYOUT_TRACE(1);
+    for (int e = tid; e < E; e += LAYOUT_THREADS) {
+        int32_t s = 0;
+#pragma unroll 4
+        for (int w = 0; w < LAYOUT_WARPS; ++w)
+            s += wcnt[w * E + e];
+        tile_counts[(int64_t)blockIdx.x * E + e] = s;
+    }
 
-    // Column sums of the tile-count table.  Thread (part, e) sums rows
-    // part, part + P, ... so all threads have loads in flight.
+    LAYOUT_TRACE(2);
+    // 2. every tile row is written
+    if (!grid_barrier(barrier, err_word))
+        return;
+    LAYOUT_TRACE(3);
+
+    // 3a. column sums of the table; thread (part, e) sums rows part, part+P, ...
     {
         const int P = E >= LAYOUT_THREADS ? 1 : LAYOUT_THREADS / E;
         const int part = tid / E;
@@ -168,7 +211,7 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
 #pragma unroll
                 for (int u = 0; u < TABLE_UNROLL; ++u) {
                     const int b = b0 + u * P;
-                    v[u] = b < tiles ? tile_counts[(int64_t)b * E + e] : 0;
+                    v[u] = b < tiles ? __ldcg(tile_counts + (int64_t)b * E + e) : 0;
                 }
 #pragma unroll
                 for (int u = 0; u < TABLE_UNROLL; ++u) {
@@ -182,52 +225,40 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
         }
     }
     __syncthreads();
+    LAYOUT_TRACE(4);
 
-    // Exclusive scan of the totals over experts (E <= 2 * LAYOUT_THREADS).
-    const int per = (E + LAYOUT_THREADS - 1) / LAYOUT_THREADS;
-    int32_t mine[2] = {0, 0};
-    int32_t sum = 0;
-    for (int q = 0; q < per; ++q) {
-        const int e = tid * per + q;
-        mine[q] = e < E ? offs[e] : 0;
-        sum += mine[q];
-    }
-    int32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t n = __shfl_up_sync(FULL_MASK, incl, o);
-        if (lane >= o)
-            incl += n;
-    }
-    if (lane == 31)
-        carry[warp] = incl;
-    __syncthreads();
+    // 3b. exclusive scan of the totals over experts, by warp 0 alone: each lane
+    //     sums a run of ceil(E/32) experts, one warp scan, each lane writes
+    //     its run's offsets (E <= MOE_MAX_EXPERTS = 1024)
     if (warp == 0) {
-        int32_t v = lane < LAYOUT_WARPS ? carry[lane] : 0;
+        const int per = (E + 31) / 32;
+        const int e0 = lane * per;
+        int32_t sum = 0;
+        for (int q = 0; q < per; ++q)
+            sum += e0 + q < E ? offs[e0 + q] : 0;
+        int32_t incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int32_t n = __shfl_up_sync(FULL_MASK, v, o);
+            const int32_t n = __shfl_up_sync(FULL_MASK, incl, o);
             if (lane >= o)
-                v += n;
+                incl += n;
         }
-        if (lane < LAYOUT_WARPS)
-            carry[lane] = v;
-    }
-    __syncthreads();
-    const int32_t total = carry[LAYOUT_WARPS - 1];
-    int32_t run = incl - sum + (warp > 0 ? carry[warp - 1] : 0);
-    for (int q = 0; q < per; ++q) {
-        const int e = tid * per + q;
-        if (e < E) {
+        int32_t run = incl - sum;
+        for (int q = 0; q < per && e0 + q < E; ++q) {
+            const int e = e0 + q;
+            const int32_t cnt = offs[e];
             offs[e] = run;
             if (blockIdx.x == 0) {
-                expert_counts[e] = mine[q];
+                expert_counts[e] = cnt;
                 expert_offsets[e] = run;
             }
+            run += cnt;
         }
-        run += mine[q];
+        if (lane == 31)
+            carry[0] = incl;
     }
     __syncthreads();
+    const int32_t total = carry[0];
     if (blockIdx.x == 0) {
         const int El = E / R;
         for (int r = tid; r <= R; r += LAYOUT_THREADS)
@@ -236,7 +267,8 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
             expert_offsets[E] = total;
     }
 
-    // Per-warp cursors: offset of e + earlier tiles + earlier warps of this tile.
+    LAYOUT_TRACE(5);
+    // 3c. per-warp cursors: offset of e + earlier tiles + earlier warps here
     for (int e = tid; e < E; e += LAYOUT_THREADS) {
         int32_t c = offs[e] + pre[e];
 #pragma unroll 4
@@ -248,7 +280,8 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
     }
     __syncthreads();
 
-    // Walk the span again and hand out slots in pair order.
+    LAYOUT_TRACE(6);
+    // 3d. walk the span again and hand out slots in pair order
     int32_t *cur = wcnt + warp * E;
     const unsigned lt = lanemask_lt();
     for (int64_t first = begin; first < end; first += 32 * LAYOUT_BATCH) {
@@ -266,7 +299,7 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
                 break;  // warp-uniform: the rest of the batch is past the span
             const int64_t i = first + b * 32 + lane;
             const int e = ev[b];
-            const unsigned peers = warp_peers(e, nbits);
+            const unsigned peers = warp_peers<NBITS>(e);
             if (e >= 0) {
                 const int32_t s = cur[e] + __popc(peers & lt);
                 slot_of[i] = s;
@@ -280,6 +313,7 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
             __syncwarp();
         }
     }
+    LAYOUT_TRACE(7);
 }
 
 // ---------------------------------------------------------------- host side
@@ -306,8 +340,7 @@ static LayoutPlan layout_plan(int64_t N)
     return p;
 }
 
-static size_t count_smem(int E) { return sizeof(int32_t) * (size_t)E; }
-static size_t assign_smem(int E)
+static size_t layout_smem(int E)
 {
     return sizeof(int32_t) * ((size_t)LAYOUT_WARPS * E + 2 * (size_t)E + LAYOUT_WARPS);
 }
@@ -317,7 +350,51 @@ size_t layout_workspace_bytes(int64_t N, int E)
     const LayoutPlan p = layout_plan(N);
     size_t bytes = sizeof(int32_t) * (size_t)p.tiles * (size_t)E;
     bytes = (bytes + 255) / 256 * 256;
-    return bytes < 256 ? 256 : bytes;
+    return LAYOUT_BARRIER_BYTES + bytes;
+}
+
+template <int NBITS>
+static cudaError_t launch_layout_t(int64_t N, int E, int R, const LayoutPlan &p,
+                                   const int32_t *topk_idx, unsigned *barrier,
+                                   int32_t *tile_counts, int32_t *expert_counts,
+                                   int32_t *expert_offsets, int32_t *rank_offsets,
+                                   int32_t *slot_of, int32_t *src_of, uint32_t *err_word,
+                                   cudaStream_t stream)
+{
+    const size_t smem = layout_smem(E);
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024)
+        e = cudaFuncSetAttribute(layout_kernel<NBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    // Cooperative: all CTAs are co-resident, as the grid barrier requires.
+    // Programmatic serialisation: the grid may become resident while the
+    // previous kernel in the stream finishes.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.tiles);
+    cfg.blockDim = dim3(LAYOUT_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS>, topk_idx, N, E, R, p.span, p.tiles, barrier,
+                           tile_counts, expert_counts, expert_offsets, rank_offsets, slot_of,
+                           src_of, err_word);
+    if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
+        // the driver refused the attribute pair: launch cooperatively only
+        (void)cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS>, topk_idx, N, E, R, p.span, p.tiles,
+                               barrier, tile_counts, expert_counts, expert_offsets, rank_offsets,
+                               slot_of, src_of, err_word);
+    }
+    return e;
 }
 
 cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
@@ -335,24 +412,33 @@ cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
         return e;
     }
     const LayoutPlan p = layout_plan(N);
-    const size_t sc = count_smem(E), sa = assign_smem(E);
     int nbits = 0;
     while ((1 << nbits) < E)
         ++nbits;
-    cudaError_t e = cudaSuccess;
-    if (sa > 48 * 1024)
-        e = cudaFuncSetAttribute(layout_assign_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
-    if (e != cudaSuccess)
-        return e;
-    int32_t *tile_counts = static_cast<int32_t *>(workspace);
-    e = launch_pdl(layout_count_kernel, dim3(p.tiles), dim3(LAYOUT_THREADS), sc, stream,
-                   topk_idx, N, E, p.span, tile_counts, err_word);
-    if (e != cudaSuccess)
-        return e;
-    return launch_pdl(layout_assign_kernel, dim3(p.tiles), dim3(LAYOUT_THREADS), sa, stream,
-                      topk_idx, N, E, R, nbits, p.span, p.tiles, tile_counts, expert_counts,
-                      expert_offsets, rank_offsets, slot_of, src_of);
+    unsigned *barrier = static_cast<unsigned *>(workspace);
+    int32_t *tile_counts = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                                       LAYOUT_BARRIER_BYTES);
+    switch (nbits) {
+#define MOE_LAYOUT_CASE(B)                                                                   \
+    case B:                                                                                  \
+        return launch_layout_t<B>(N, E, R, p, topk_idx, barrier, tile_counts, expert_counts, \
+                                  expert_offsets, rank_offsets, slot_of, src_of, err_word,   \
+                                  stream);
+        MOE_LAYOUT_CASE(0)
+        MOE_LAYOUT_CASE(1)
+        MOE_LAYOUT_CASE(2)
+        MOE_LAYOUT_CASE(3)
+        MOE_LAYOUT_CASE(4)
+        MOE_LAYOUT_CASE(5)
+        MOE_LAYOUT_CASE(6)
+        MOE_LAYOUT_CASE(7)
+        MOE_LAYOUT_CASE(8)
+        MOE_LAYOUT_CASE(9)
+        MOE_LAYOUT_CASE(10)
+#undef MOE_LAYOUT_CASE
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace moe

@@ -14,9 +14,10 @@
 // cudaGetSymbolAddress and caches it; make that first call before any stream
 // capture.  All calls on a device share the one array: calls whose kernels
 // overlap on the GPU (different streams, no ordering between them) race on it.
-// Nothing in it has to start at zero: the count kernel rewrites every entry the
-// assign kernel reads.  The entry point allocates nothing, frees nothing and
-// calls no allocating library routine.
+// Only its first 8 bytes (the layout kernel's grid barrier) must start at
+// zero, and each call clears them on the stream before launching; the tile
+// table is rewritten before it is read.  The entry point allocates nothing,
+// frees nothing and calls no allocating library routine.
 #include <mutex>
 
 #include "launch.h"
@@ -76,8 +77,11 @@ extern "C" MOE_API moe_status moe_layout_noalloc(int T, int k, int E, int R,
     void *scratch = scratch_on_current_device();
     if (scratch == nullptr)
         return MOE_ERR_CUDA;
-    const cudaError_t e =
-        moe::launch_layout(T, k, E, R, topk_idx, expert_counts, expert_offsets, rank_offsets,
-                           slot_of, src_of, scratch, err_word, stream);
+    // The layout kernel's grid barrier (the array's first 8 bytes) must start
+    // at zero; clear it on the stream so no earlier failure can leave it set.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, 8, stream);
+    if (e == cudaSuccess)
+        e = moe::launch_layout(T, k, E, R, topk_idx, expert_counts, expert_offsets, rank_offsets,
+                               slot_of, src_of, scratch, err_word, stream);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -67,8 +67,12 @@ MOE_API const char *moe_status_string(int status);
 
 /*
  * Bytes of device workspace moe_layout needs for (T, k, E); 0 for bad sizes.
- * The workspace holds per-tile expert counts; its contents need no
- * initialisation and are scratch between calls.
+ * The first 256 bytes hold the grid barrier of the layout kernel (one
+ * cooperative launch): zero-fill the workspace once before its first use.
+ * Every successful call leaves the barrier's arrival count at zero again, so
+ * it never needs zeroing again (after MOE_ERR_TIMEOUT, zero it again).  The
+ * rest holds per-tile expert counts, scratch between calls.  One workspace
+ * serves any (T, k, E) whose size fits.
  */
 MOE_API size_t moe_layout_workspace_bytes(int T, int k, int E);
 
@@ -88,7 +92,8 @@ MOE_API size_t moe_layout_workspace_bytes(int T, int k, int E);
  *                          segment of the receive buffer; [R] = T*k
  *   slot_of         [T, k] out: receive-buffer row of (t, j)
  *   src_of          [T*k]  out: inverse map, src_of[slot_of[t,j]] = t*k + j
- *   workspace       moe_layout_workspace_bytes(T, k, E) bytes of device scratch
+ *   workspace       moe_layout_workspace_bytes(T, k, E) bytes of device scratch,
+ *                   zero-filled before its first use (see above)
  *
  * Slot order is (rank, expert, token, j): rank-segmented, expert-contiguous,
  * and stable in (t, j), with no padding.  The result is deterministic and
@@ -177,7 +182,8 @@ MOE_API moe_status moe_combine(int T, int H, int k, const void *y, const int32_t
  * device address; make that first call before any stream capture.  All calls
  * on one device share the array and its contents persist between calls:
  * calls whose work overlaps on the GPU (unordered streams) race on it.
- * Nothing in it needs zeroing.  Requests whose count table would exceed
+ * Each call clears the part that must start at zero (8 bytes, on the
+ * stream), so the caller never clears anything.  Requests whose count table would exceed
  * MOE_NOALLOC_SCRATCH_BYTES (more than 512 experts with the largest token
  * counts) return MOE_ERR_UNSUPPORTED without launching; moe_layout handles
  * them.  The call allocates and frees nothing.

@@ -47,12 +47,12 @@ def test_status_strings_and_version(m):
 
 def test_workspace_bytes(m):
     assert m.moe_layout_workspace_bytes(1024, 8, 256) >= 256
-    assert m.moe_layout_workspace_bytes(0, 8, 256) == 256
+    assert m.moe_layout_workspace_bytes(0, 8, 256) == 256      # the barrier counter only
     assert m.moe_layout_workspace_bytes(-1, 8, 256) == 0
     assert m.moe_layout_workspace_bytes(1 << 28, 8, 256) == 0      # T*k >= 2^31
     assert m.moe_layout_workspace_bytes(16, 2, 4096) == 0          # E above the maximum
-    # grows with the tile count, capped at 128 tiles x E int32
-    assert m.moe_layout_workspace_bytes(1 << 20, 8, 256) == 128 * 256 * 4
+    # barrier counter + tile table, capped at 128 tiles x E int32
+    assert m.moe_layout_workspace_bytes(1 << 20, 8, 256) == 256 + 128 * 256 * 4
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced
