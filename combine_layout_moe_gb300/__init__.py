@@ -36,6 +36,9 @@ SIGNATURES = {
     "moe_combine": ([_I, _I, _I, _P, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_read_error": ([_U32P, _I, _P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "moe_layout_noalloc": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
+    "moe_flag_words": ([_I, _I, _I], ctypes.c_size_t),
+    "moe_dispatch_combine_flagged": ([_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_uint32,
+                                      ctypes.c_uint64, ctypes.c_int64, _U32P, _P], ctypes.c_int),
 }
 
 
@@ -219,6 +222,53 @@ def moe_combine(y: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.Tensor, *,
     return out
 
 
+def moe_flag_words(T: int, H: int, k: int) -> int:
+    return int(_lib.moe_flag_words(T, H, k))
+
+
+class FlagWords:
+    """Sequence words for moe_dispatch_combine_flagged: zero-filled once, and a
+    fresh epoch (1, 2, 3, ...) for every call that reuses them."""
+
+    def __init__(self, T: int, H: int, k: int, device=None):
+        self.words = torch.zeros(max(moe_flag_words(T, H, k), 1), dtype=torch.int32,
+                                 device=device or "cuda")
+        self.epoch = 0
+
+    def next_epoch(self) -> int:
+        self.epoch = (self.epoch % 0xFFFFFFFF) + 1
+        return self.epoch
+
+
+def moe_dispatch_combine_flagged(x: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.Tensor,
+                                 flags: FlagWords, *, out_dtype: torch.dtype = torch.bfloat16,
+                                 recv: Optional[torch.Tensor] = None,
+                                 out: Optional[torch.Tensor] = None,
+                                 spin_limit_ns: int = 1_000_000_000, fault_skip_pair: int = -1,
+                                 err_word: Optional[torch.Tensor] = None,
+                                 stream: Optional[torch.cuda.Stream] = None):
+    """Dispatch, identity expert and combine in one persistent kernel with
+    per-row-chunk readiness words.  Returns (recv, out)."""
+    T, H = x.shape
+    k = slot_of.shape[1]
+    _want(x, "x", torch.bfloat16)
+    _want(slot_of, "slot_of", torch.int32, (T, k))
+    _want(topk_w, "topk_w", torch.float32, (T, k))
+    if recv is None:
+        recv = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=x.device)
+    _want(recv, "recv", torch.bfloat16, (T * k, H))
+    _want(out, "out", out_dtype, (T, H))
+    code = MOE_OUT_BF16 if out_dtype == torch.bfloat16 else MOE_OUT_F32
+    _check(_lib.moe_dispatch_combine_flagged(T, H, k, _ptr(x), _ptr(slot_of), _ptr(topk_w),
+                                             _ptr(recv), _ptr(out), code, _ptr(flags.words),
+                                             flags.next_epoch(), int(spin_limit_ns),
+                                             int(fault_skip_pair), _ptr(err_word),
+                                             _stream(stream)), "moe_dispatch_combine_flagged")
+    return recv, out
+
+
 def moe_read_error(err_word: torch.Tensor, clear: bool = True,
                    stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronise, read (and clear) the error word; returns the error bits."""
@@ -233,5 +283,6 @@ def moe_read_error(err_word: torch.Tensor, clear: bool = True,
 __all__ = [
     "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word", "new_workspace",
     "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
-    "moe_combine", "moe_read_error", "LIB_PATH", "SIGNATURES",
+    "moe_combine", "moe_read_error", "moe_flag_words", "FlagWords",
+    "moe_dispatch_combine_flagged", "LIB_PATH", "SIGNATURES",
 ]

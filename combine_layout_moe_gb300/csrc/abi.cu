@@ -153,6 +153,35 @@ moe_status moe_combine(int T, int H, int k, const void *y, const int32_t *slot_o
                                          out_dtype == MOE_OUT_F32, err_word, stream));
 }
 
+size_t moe_flag_words(int T, int H, int k)
+{
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0)
+        return 0;
+    return (size_t)T * k * (size_t)moe::flagged_chunks(H);
+}
+
+moe_status moe_dispatch_combine_flagged(int T, int H, int k, const void *x, const int32_t *slot_of,
+                                        const float *topk_w, void *recv, void *out, int out_dtype,
+                                        uint32_t *seq, uint32_t epoch, uint64_t spin_limit_ns,
+                                        int64_t fault_skip_pair, uint32_t *err_word,
+                                        cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0 || epoch == 0 || spin_limit_ns == 0)
+        return MOE_ERR_INVALID_ARG;
+    if (k > 32)
+        return MOE_ERR_UNSUPPORTED;
+    if (out_dtype != MOE_OUT_BF16 && out_dtype != MOE_OUT_F32)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !slot_of || !topk_w || !recv || !out || !seq))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(out, 16) || !aligned(slot_of, 4) ||
+        !aligned(topk_w, 4) || !aligned(seq, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_dispatch_combine_flagged(
+        T, H, k, x, slot_of, topk_w, recv, out, out_dtype == MOE_OUT_F32, seq, epoch, spin_limit_ns,
+        fault_skip_pair, err_word, stream));
+}
+
 moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t stream, uint32_t *bits_out)
 {
     if (!err_word || !aligned(err_word, 4))

@@ -26,6 +26,15 @@ cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *sl
                            const float *topk_w, void *out, bool out_f32,
                            uint32_t *err_word, cudaStream_t stream);
 
+int flagged_chunks(int H);
+
+cudaError_t launch_dispatch_combine_flagged(int T, int H, int k, const void *x,
+                                            const int32_t *slot_of, const float *topk_w,
+                                            void *recv, void *out, bool out_f32, uint32_t *seq,
+                                            uint32_t epoch, uint64_t spin_limit_ns,
+                                            int64_t skip_pair, uint32_t *err_word,
+                                            cudaStream_t stream);
+
 // Launches `kernel` on `stream` with programmatic stream serialisation, so it
 // may become resident while the previous kernel in the stream is still running
 // (the kernel itself waits for that grid before touching global memory).

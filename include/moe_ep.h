@@ -166,6 +166,41 @@ MOE_API moe_status moe_combine(int T, int H, int k, const void *y, const int32_t
                        cudaStream_t stream);
 
 /*
+ * moe_dispatch_combine_flagged -- dispatch, an identity expert and combine in
+ * one persistent kernel, with Data-as-Flag readiness instead of a barrier.
+ *
+ * UBEP, section 3.4 (Data-as-Flag: readiness travels with the data), section
+ * 3.2 (consumers start as soon as their inputs are signalled) and section 6
+ * (without atomic 512-byte writes, fall back to explicit fences).  Producers
+ * copy each token's row chunk to its k slots, fence, and set one 32-bit
+ * sequence word per (slot row, chunk) to `epoch`; consumers wait for the words
+ * of a token's k rows (acquire loads, bounded by spin_limit_ns), read the rows
+ * back and reduce them as moe_combine does.  Results: recv as moe_dispatch,
+ * out = moe_combine(recv, slot_of, topk_w) (the identity expert).
+ *
+ *   seq       moe_flag_words(T, H, k) uint32 device words, zero-filled once;
+ *             none may already hold `epoch`
+ *   epoch     non-zero and different on every call that reuses `seq`
+ *             (e.g. 1, 2, 3, ...)
+ *   spin_limit_ns   bound on each wait; a wait that runs out sets
+ *             MOE_ERRBIT_TIMEOUT, that token chunk's output is left unwritten,
+ *             and the kernel still returns
+ *   fault_skip_pair test hook: the producer of pair t*k+j == fault_skip_pair
+ *             does not set its word, so the matching consumer's wait runs out;
+ *             pass -1 in normal use
+ *
+ * One cooperative launch (every CTA resident).  1 <= k <= 32; H % 8 == 0.
+ */
+MOE_API size_t moe_flag_words(int T, int H, int k);
+
+MOE_API moe_status moe_dispatch_combine_flagged(int T, int H, int k, const void *x,
+                                        const int32_t *slot_of, const float *topk_w,
+                                        void *recv, void *out, int out_dtype, uint32_t *seq,
+                                        uint32_t epoch, uint64_t spin_limit_ns,
+                                        int64_t fault_skip_pair, uint32_t *err_word,
+                                        cudaStream_t stream);
+
+/*
  * moe_layout_noalloc -- moe_layout for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a deployment convenience.
  *

@@ -96,3 +96,11 @@ def test_payload_calls_reject_bad_shapes_and_alignment(m):
     assert L.moe_combine(4, 64, 2, FAKE, FAKE, FAKE, FAKE + 8, 0, None, None) == bad
     assert L.moe_combine(4, 64, 0, FAKE, FAKE, FAKE, FAKE, 0, None, None) == bad
     assert L.moe_read_error(None, 1, None, None) == bad
+    # flagged variant: epoch 0, zero spin limit, k above 32
+    assert L.moe_dispatch_combine_flagged(4, 64, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 10,
+                                          -1, None, None) == bad
+    assert L.moe_dispatch_combine_flagged(4, 64, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 0,
+                                          -1, None, None) == bad
+    assert L.moe_dispatch_combine_flagged(4, 64, 40, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 10,
+                                          -1, None, None) == m.MOE_ERR_UNSUPPORTED
+    assert m.moe_flag_words(1024, 7168, 8) == 1024 * 8 * 7
