@@ -160,6 +160,22 @@ __device__ __forceinline__ void advance(int64_t &t, int &c, int step, int nchunk
     }
 }
 
+// Per-CTA timestamps for tuning builds (-DMOE_TRACE): slot 8 + 4*cta + i of
+// the 64-bit words after the error word (0 start, 1 first stage landed,
+// 2 consumers done).
+#ifdef MOE_TRACE
+#define CT_TRACE(i)                                                                   \
+    do {                                                                              \
+        if (err_word)                                                                 \
+            reinterpret_cast<unsigned long long *>(err_word)[8 + 4 * blockIdx.x + (i)] = \
+                global_ns();                                                          \
+    } while (0)
+#else
+#define CT_TRACE(i) \
+    do {            \
+    } while (0)
+#endif
+
 template <int KMAX>
 __global__ void __launch_bounds__(CT_THREADS, 1)
     combine_bulk_kernel(const uint8_t *__restrict__ y, const int32_t *__restrict__ slot_of,
@@ -188,6 +204,8 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
     __syncthreads();
     wait_prior_grid();
     allow_next_grid();
+    if (threadIdx.x == 0)
+        CT_TRACE(0);
 
     // this CTA's contiguous range of units (unit = token t, chunk c)
     const int64_t u0 = units * blockIdx.x / gridDim.x;
@@ -272,6 +290,8 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                 report(err_word, MOE_ERRBIT_TIMEOUT);
             return;
         }
+        if (n == 0 && lane == 0)
+            CT_TRACE(1);
         const float *h = hdr + s * CT_HDR_WORDS;
         const unsigned okmask = reinterpret_cast<const uint32_t *>(h)[32];
         float w[KMAX];
@@ -319,6 +339,11 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         if (lane == 0)
             mbar_arrive(empty(s));
     }
+#ifdef MOE_TRACE
+    if (lane == 0)
+        atomicMax(reinterpret_cast<unsigned long long *>(err_word) + 8 + 4 * blockIdx.x + 2,
+                  (unsigned long long)global_ns());
+#endif
 }
 
 template <int KMAX>
