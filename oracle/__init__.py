@@ -53,8 +53,11 @@ def _bind(path: str) -> ctypes.CDLL:
     L.oracle_e4m3_encode_array.restype = None
     L.oracle_f32_to_bf16_array.argtypes = [P, P, ctypes.c_int64]
     L.oracle_f32_to_bf16_array.restype = None
+    L.oracle_combine_backward.argtypes = [I, I, I, P, P, P, P, P, P, P]
+    L.oracle_dispatch_backward.argtypes = [I, I, I, P, P, P, I]
     for f in ("oracle_layout", "oracle_dispatch", "oracle_dispatch_quant",
-              "oracle_combine", "oracle_combine_f64", "oracle_abi_version"):
+              "oracle_combine", "oracle_combine_f64", "oracle_abi_version",
+              "oracle_combine_backward", "oracle_dispatch_backward"):
         getattr(L, f).restype = ctypes.c_int
     return L
 
@@ -161,6 +164,39 @@ def combine_f64(y_bf16: np.ndarray, slot_of: np.ndarray, topk_w: np.ndarray):
     mag = np.empty((T, H), np.float64)
     _check(lib().oracle_combine_f64(T, H, k, _p(y), _p(so), _p(w), _p(out), _p(mag)))
     return out, mag
+
+
+def combine_backward(dout_bf16: np.ndarray, y_bf16, slot_of: np.ndarray, topk_w: np.ndarray):
+    """Returns (dy uint16 bf16 bits [T*k, H], dw float64 [T,k] or None,
+    dw_abs_sum float64 [T,k] or None).  y may be None (no dw)."""
+    d = np.ascontiguousarray(dout_bf16, dtype=np.uint16)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    T, H = d.shape
+    k = so.shape[1]
+    dy = np.empty((T * k, H), np.uint16)
+    if y_bf16 is None:
+        _check(lib().oracle_combine_backward(T, H, k, _p(d), None, _p(so), _p(w), _p(dy), None,
+                                             None))
+        return dy, None, None
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    dw = np.empty((T, k), np.float64)
+    mag = np.empty((T, k), np.float64)
+    _check(lib().oracle_combine_backward(T, H, k, _p(d), _p(y), _p(so), _p(w), _p(dy), _p(dw),
+                                         _p(mag)))
+    return dy, dw, mag
+
+
+def dispatch_backward(drecv_bf16: np.ndarray, slot_of: np.ndarray, out_dtype: str = "bf16"):
+    """dx[t] = sum_j drecv[slot_of[t,j]]; uint16 bf16 bits or float32 [T, H]."""
+    dr = np.ascontiguousarray(drecv_bf16, dtype=np.uint16)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    T, k = so.shape
+    H = dr.shape[1]
+    out = np.empty((T, H), np.uint16 if out_dtype == "bf16" else np.float32)
+    _check(lib().oracle_dispatch_backward(T, H, k, _p(dr), _p(so), _p(out),
+                                          0 if out_dtype == "bf16" else 1))
+    return out
 
 
 def e4m3_encode(f: np.ndarray) -> np.ndarray:

@@ -20,6 +20,10 @@
  *   oracle_combine         float64 closed form within the fp32 error bound, one-hot
  *                          weights, identity-expert round trip
  *   oracle_f32_to_bf16     torch bfloat16 cast
+ *   oracle_combine_backward  torch autograd of a float64 forward combine; torch's
+ *                          bf16 rounding of fp32 products; numpy einsum for dw
+ *   oracle_dispatch_backward oracle_combine with unit weights (special case),
+ *                          float64 closed form within the fp32 bound
  */
 #include <float.h>
 #include <math.h>
@@ -309,6 +313,79 @@ int oracle_combine_f64(int T, int H, int k, const uint16_t *y, const int32_t *sl
             out[(int64_t)t * H + h] = acc;
             if (abs_sum)
                 abs_sum[(int64_t)t * H + h] = mag;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Backward pass.  HyperParallel-MoE section 2.2 / Figure 2(b): the backward   */
+/* Dispatch is the gradient of the forward Combine, and the backward Combine   */
+/* returns the input-activation gradient (the gradient of the forward          */
+/* Dispatch).  With out[t] = sum_j w[t,j] * y[slot_of[t,j]]:                   */
+/*   dy[slot_of[t,j]] = w[t,j] * dout[t]  (one fp32 multiply, rounded to bf16) */
+/*   dw[t,j]          = <y[slot_of[t,j]], dout[t]>  (returned in binary64:     */
+/*                      bf16 x bf16 products are exact, so this is the exact   */
+/*                      value up to binary64 rounding; abs_sum bounds the fp32 */
+/*                      summation error of an implementation)                  */
+/* and with recv[slot_of[t,j]] = x[t]:                                         */
+/*   dx[t] = sum_j drecv[slot_of[t,j]]  (fp32, slots in order, from +0)        */
+/* ------------------------------------------------------------------------- */
+int oracle_combine_backward(int T, int H, int k, const uint16_t *dout, const uint16_t *y,
+                            const int32_t *slot_of, const float *topk_w, uint16_t *dy,
+                            double *dw, double *dw_abs_sum)
+{
+    if (T < 0 || H < 1 || k < 1)
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    for (int t = 0; t < T; ++t) {
+        const uint16_t *d = dout + (int64_t)t * H;
+        for (int j = 0; j < k; ++j) {
+            int64_t i = (int64_t)t * k + j;
+            int32_t s = slot_of[i];
+            if (s < 0 || s >= N)
+                return ORACLE_ERR_BAD_INDEX;
+            const float w = topk_w[i];
+            double acc = 0.0, mag = 0.0;
+            for (int h = 0; h < H; ++h) {
+                const float dv = bf16_to_f32(d[h]);
+                const float prod = w * dv;
+                dy[(int64_t)s * H + h] = oracle_f32_to_bf16(prod);
+                if (y) {
+                    const double p = (double)bf16_to_f32(y[(int64_t)s * H + h]) * (double)dv;
+                    acc += p;
+                    mag += fabs(p);
+                }
+            }
+            if (dw)
+                dw[i] = acc;
+            if (dw_abs_sum)
+                dw_abs_sum[i] = mag;
+        }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_dispatch_backward(int T, int H, int k, const uint16_t *drecv, const int32_t *slot_of,
+                             void *dx, int out_dtype)
+{
+    if (T < 0 || H < 1 || k < 1 || (out_dtype != 0 && out_dtype != 1))
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int32_t s = slot_of[(int64_t)t * k + j];
+            if (s < 0 || s >= N)
+                return ORACLE_ERR_BAD_INDEX;
+        }
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j)
+                acc = acc + bf16_to_f32(drecv[(int64_t)slot_of[(int64_t)t * k + j] * H + h]);
+            if (out_dtype == 0)
+                ((uint16_t *)dx)[(int64_t)t * H + h] = oracle_f32_to_bf16(acc);
+            else
+                ((float *)dx)[(int64_t)t * H + h] = acc;
         }
     }
     return ORACLE_OK;

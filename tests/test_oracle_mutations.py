@@ -10,6 +10,7 @@ import test_oracle_combine as tc
 import test_oracle_dispatch as td
 import test_oracle_layout as tl
 import test_oracle_bf16 as tb
+import test_oracle_backward as tbw
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "moe_oracle.c")
@@ -33,6 +34,12 @@ MUTANTS = {
                       "float v = bf16_to_f32(y[(int64_t)slot_of[(int64_t)t * k] * H + h]);"),
     # combine: weight and value of neighbouring slots swapped
     "combine_weight": ("acc = fmaf(topk_w[i], v, acc);", "acc = fmaf(topk_w[(int64_t)t * k + (j + 1) % k], v, acc);"),
+    # backward: dy scaled by the weight of the wrong slot
+    "dy_weight": ("const float w = topk_w[i];\n            double acc = 0.0, mag = 0.0;",
+                  "const float w = topk_w[(int64_t)t * k];\n            double acc = 0.0, mag = 0.0;"),
+    # backward: dx skips the last slot
+    "dx_drop": ("            for (int j = 0; j < k; ++j)\n                acc = acc + bf16_to_f32(",
+                "            for (int j = 0; j + 1 < k; ++j)\n                acc = acc + bf16_to_f32("),
     # bf16: ties rounded up instead of to even
     "bf16_ties": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (lower >= 0x8000u)"),
 }
@@ -52,7 +59,9 @@ def _pins():
              lambda: td.test_dispatch_rows_equal_source_token(("fuzz", 0)),
              tc.test_one_hot_weights_select_one_slot, tc.test_weights_are_not_renormalised,
              lambda: tc.test_bf16_output_is_rounded_fp32_output("fuzz0", None),
-             tb.test_random_and_special_values_match_torch]
+             tb.test_random_and_special_values_match_torch,
+             lambda: tbw.test_combine_backward_matches_autograd(tbw.CASES[1]),
+             lambda: tbw.test_dispatch_backward_is_unit_weight_combine(tbw.CASES[1])]
     return pins
 
 
