@@ -37,6 +37,8 @@ SIGNATURES = {
     "moe_read_error": ([_U32P, _I, _P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "moe_layout_noalloc": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_flag_words": ([_I, _I, _I], ctypes.c_size_t),
+    "moe_combine_backward": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
+    "moe_dispatch_backward": ([_I, _I, _I, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_dispatch_combine_flagged": ([_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_uint32,
                                       ctypes.c_uint64, ctypes.c_int64, _U32P, _P], ctypes.c_int),
 }
@@ -222,6 +224,51 @@ def moe_combine(y: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.Tensor, *,
     return out
 
 
+def moe_combine_backward(dout: torch.Tensor, y: Optional[torch.Tensor], slot_of: torch.Tensor,
+                         topk_w: torch.Tensor, *, dy: Optional[torch.Tensor] = None,
+                         dw: Optional[torch.Tensor] = None, want_dw: bool = True,
+                         err_word: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None):
+    """Gradient of moe_combine.  Returns (dy bf16 [T*k, H], dw fp32 [T, k] or None)."""
+    T, H = dout.shape
+    k = slot_of.shape[1]
+    _want(dout, "dout", torch.bfloat16)
+    _want(slot_of, "slot_of", torch.int32, (T, k))
+    _want(topk_w, "topk_w", torch.float32, (T, k))
+    if y is not None:
+        _want(y, "y", torch.bfloat16, (T * k, H))
+    if dy is None:
+        dy = torch.empty((T * k, H), dtype=torch.bfloat16, device=dout.device)
+    _want(dy, "dy", torch.bfloat16, (T * k, H))
+    if want_dw and y is not None and dw is None:
+        dw = torch.empty((T, k), dtype=torch.float32, device=dout.device)
+    if not want_dw or y is None:
+        dw = None
+    _check(_lib.moe_combine_backward(T, H, k, _ptr(dout), _ptr(y), _ptr(slot_of), _ptr(topk_w),
+                                     _ptr(dy), _ptr(dw), _ptr(err_word), _stream(stream)),
+           "moe_combine_backward")
+    return dy, dw
+
+
+def moe_dispatch_backward(drecv: torch.Tensor, slot_of: torch.Tensor, *,
+                          out_dtype: torch.dtype = torch.bfloat16,
+                          dx: Optional[torch.Tensor] = None,
+                          err_word: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Gradient of moe_dispatch: dx[t] = sum_j drecv[slot_of[t, j]]."""
+    T, k = slot_of.shape
+    H = drecv.shape[1]
+    _want(drecv, "drecv", torch.bfloat16, (T * k, H))
+    _want(slot_of, "slot_of", torch.int32)
+    if dx is None:
+        dx = torch.empty((T, H), dtype=out_dtype, device=drecv.device)
+    _want(dx, "dx", out_dtype, (T, H))
+    code = MOE_OUT_BF16 if out_dtype == torch.bfloat16 else MOE_OUT_F32
+    _check(_lib.moe_dispatch_backward(T, H, k, _ptr(drecv), _ptr(slot_of), _ptr(dx), code,
+                                      _ptr(err_word), _stream(stream)), "moe_dispatch_backward")
+    return dx
+
+
 def moe_flag_words(T: int, H: int, k: int) -> int:
     return int(_lib.moe_flag_words(T, H, k))
 
@@ -284,5 +331,6 @@ __all__ = [
     "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word", "new_workspace",
     "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
     "moe_combine", "moe_read_error", "moe_flag_words", "FlagWords",
+    "moe_combine_backward", "moe_dispatch_backward",
     "moe_dispatch_combine_flagged", "LIB_PATH", "SIGNATURES",
 ]

@@ -153,6 +153,39 @@ moe_status moe_combine(int T, int H, int k, const void *y, const int32_t *slot_o
                                          out_dtype == MOE_OUT_F32, err_word, stream));
 }
 
+moe_status moe_combine_backward(int T, int H, int k, const void *dout, const void *y,
+                                const int32_t *slot_of, const float *topk_w, void *dy, float *dw,
+                                uint32_t *err_word, cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (k > 32)
+        return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!dout || !slot_of || !topk_w || !dy || (dw && !y)))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(dout, 16) || !aligned(y, 16) || !aligned(dy, 16) || !aligned(slot_of, 4) ||
+        !aligned(topk_w, 4) || !aligned(dw, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine_backward(T, H, k, dout, y, slot_of, topk_w, dy, dw,
+                                                  err_word, stream));
+}
+
+moe_status moe_dispatch_backward(int T, int H, int k, const void *drecv, const int32_t *slot_of,
+                                 void *dx, int out_dtype, uint32_t *err_word, cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (out_dtype != MOE_OUT_BF16 && out_dtype != MOE_OUT_F32)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!drecv || !slot_of || !dx))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(drecv, 16) || !aligned(dx, 16) || !aligned(slot_of, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    // the combine pipeline with unit weights
+    return from_cuda(moe::launch_combine(T, H, k, drecv, slot_of, nullptr, dx,
+                                         out_dtype == MOE_OUT_F32, err_word, stream));
+}
+
 size_t moe_flag_words(int T, int H, int k)
 {
     if (!pairs_ok(T, k) || H < 8 || H % 8 != 0)

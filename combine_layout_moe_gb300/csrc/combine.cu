@@ -54,13 +54,13 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2)
                 acc[u][i] = 0.0f;
 
         const int32_t *so = slot_of + t * k;
-        const float *wt = topk_w + t * k;
+        const float *wt = topk_w ? topk_w + t * k : nullptr;
         int32_t my_slot = 0;
         float my_w = 0.0f;
         for (int jb = 0; jb < k; jb += KC) {
             if ((jb & 31) == 0) {
                 my_slot = jb + lane < k ? ld_nc_s32(so + jb + lane) : 0;
-                my_w = jb + lane < k ? ld_nc_f32(wt + jb + lane) : 0.0f;
+                my_w = jb + lane < k ? (topk_w ? ld_nc_f32(wt + jb + lane) : 1.0f) : 0.0f;
             }
             uint4 v[KC][U];
             bool ok[KC];
@@ -219,11 +219,15 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         int64_t t = u0 / nchunks;
         int c = (int)(u0 - t * nchunks);
         const bool kl = lane < k;
+        // a null weight array means unit weights (the gradient of dispatch)
+        auto weight = [&](int64_t tok) {
+            return topk_w ? ld_nc_f32(topk_w + tok * k + lane) : 1.0f;
+        };
         int32_t cur_slot = kl ? ld_nc_s32(slot_of + t * k + lane) : 0;
-        float cur_w = kl ? ld_nc_f32(topk_w + t * k + lane) : 0.0f;
+        float cur_w = kl ? weight(t) : 0.0f;
         const bool has_next = t + 1 < T;
         int32_t nxt_slot = kl && has_next ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
-        float nxt_w = kl && has_next ? ld_nc_f32(topk_w + (t + 1) * k + lane) : 0.0f;
+        float nxt_w = kl && has_next ? weight(t + 1) : 0.0f;
         int64_t n = 0;
         bool timed_out = false;
         for (; n < nloc; ++n) {
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                     cur_w = nxt_w;
                     const bool more = kl && t + 1 < T;
                     nxt_slot = more ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
-                    nxt_w = more ? ld_nc_f32(topk_w + (t + 1) * k + lane) : 0.0f;
+                    nxt_w = more ? weight(t + 1) : 0.0f;
                 }
             }
             const int s = (int)(n % CT_STAGES);
@@ -392,6 +396,137 @@ static cudaError_t launch_combine_t(int T, int H, int k, const void *y, const in
     return launch_pdl(combine_kernel<KC, U>, dim3(grid), dim3(COMBINE_THREADS), 0, stream,
                       static_cast<const uint4 *>(y), slot_of, topk_w, out, out_f32 ? 1 : 0, k, C,
                       groups, items, T * k, err_word);
+}
+
+// ---------------------------------------------------------------- backward
+//
+// HyperParallel-MoE, section 2.2 / Figure 2(b): the backward Dispatch is the
+// gradient of the forward Combine.  One CTA per token: its 8 warps take equal
+// slices of the row; per 16-byte vector a lane loads dout and the k rows of y
+// (KMAX / 8 groups of 8 loads in flight), stores the k scaled copies
+// dy[slot_of[t,j]] = bf16(w[t,j] * dout[t]) (one fp32 multiply, one rounding)
+// and accumulates the k dot products <y[slot_of[t,j]], dout[t]> in fp32.  The
+// partial dot products are reduced in a fixed order (xor-shuffle tree, then
+// the warps in index order through shared memory): deterministic.
+constexpr int CB_WARPS = 8;
+
+template <int KMAX>
+__global__ void __launch_bounds__(32 * CB_WARPS)
+    combine_backward_kernel(const uint4 *__restrict__ dout, const uint4 *__restrict__ y,
+                            const int32_t *__restrict__ slot_of, const float *__restrict__ topk_w,
+                            uint4 *__restrict__ dy, float *__restrict__ dw, int T, int k, int C,
+                            uint32_t *err_word)
+{
+    __shared__ float red[CB_WARPS][KMAX];
+    wait_prior_grid();
+    allow_next_grid();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int N = T * k;
+    const int per = (C + CB_WARPS - 1) / CB_WARPS;
+    const int c0 = warp * per, c1 = min(C, c0 + per);
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const int32_t ms = lane < k ? ld_nc_s32(slot_of + t * k + lane) : -1;
+        const float mw = lane < k ? ld_nc_f32(topk_w + t * k + lane) : 0.0f;
+        const unsigned okmask = __ballot_sync(FULL_MASK, lane < k && (unsigned)ms < (unsigned)N);
+        if (warp == 0 && lane == 0 && okmask != (k >= 32 ? FULL_MASK : ((1u << k) - 1u)))
+            report(err_word, MOE_ERRBIT_BAD_INDEX);
+        float part[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            part[j] = 0.0f;
+        // warp-uniform loop (the shuffles below need every lane); a lane past
+        // the slice only skips its loads, arithmetic and stores
+        for (int cb = c0; cb < c1; cb += 32) {
+            const int c = cb + lane;
+            const bool act = c < c1;
+            const uint4 d = act ? ld_stream_v4(dout + t * C + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t dw4[4] = {d.x, d.y, d.z, d.w};
+            float df[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                df[2 * h] = bf16lo(dw4[h]);
+                df[2 * h + 1] = bf16hi(dw4[h]);
+            }
+#pragma unroll
+            for (int jb = 0; jb < KMAX; jb += 8) {
+                if (jb >= k)
+                    break;
+                uint4 yv[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = jb + q;
+                    const int32_t s = __shfl_sync(FULL_MASK, ms, j & 31);
+                    yv[q] = (act && y && j < k && ((okmask >> j) & 1u))
+                                ? ld_stream_v4(y + (int64_t)s * C + c)
+                                : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = jb + q;
+                    const int32_t s = __shfl_sync(FULL_MASK, ms, j & 31);
+                    const float w = __shfl_sync(FULL_MASK, mw, j & 31);
+                    if (!act || j >= k || !((okmask >> j) & 1u))
+                        continue;
+                    const uint32_t yw[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
+                    uint32_t r[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        part[j] = __fmaf_rn(bf16lo(yw[h]), df[2 * h], part[j]);
+                        part[j] = __fmaf_rn(bf16hi(yw[h]), df[2 * h + 1], part[j]);
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(w, df[2 * h]),
+                                                                       __fmul_rn(w, df[2 * h + 1]));
+                        r[h] = *reinterpret_cast<const uint32_t *>(&b);
+                    }
+                    st_v4(dy + (int64_t)s * C + c, make_uint4(r[0], r[1], r[2], r[3]));
+                }
+            }
+        }
+        if (dw) {
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                float v = part[j];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1)
+                    v += __shfl_xor_sync(FULL_MASK, v, o);
+                if (lane == 0)
+                    red[warp][j] = v;
+            }
+            __syncthreads();
+            if (warp == 0 && lane < k) {
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < CB_WARPS; ++w)
+                    v += red[w][lane];
+                dw[t * k + lane] = v;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <int KMAX>
+static cudaError_t launch_combine_backward_t(int T, int H, int k, const void *dout, const void *y,
+                                             const int32_t *slot_of, const float *topk_w,
+                                             void *dy, float *dw, uint32_t *err_word,
+                                             cudaStream_t stream)
+{
+    const int64_t g = T < 65535 * 32 ? T : 65535 * 32;
+    return launch_pdl(combine_backward_kernel<KMAX>, dim3((unsigned)g), dim3(32 * CB_WARPS), 0,
+                      stream, static_cast<const uint4 *>(dout), static_cast<const uint4 *>(y),
+                      slot_of, topk_w, static_cast<uint4 *>(dy), dw, T, k, H / 8, err_word);
+}
+
+cudaError_t launch_combine_backward(int T, int H, int k, const void *dout, const void *y,
+                                    const int32_t *slot_of, const float *topk_w, void *dy,
+                                    float *dw, uint32_t *err_word, cudaStream_t stream)
+{
+    if (T == 0)
+        return cudaSuccess;
+    if (k <= 8)
+        return launch_combine_backward_t<8>(T, H, k, dout, y, slot_of, topk_w, dy, dw, err_word,
+                                            stream);
+    return launch_combine_backward_t<32>(T, H, k, dout, y, slot_of, topk_w, dy, dw, err_word,
+                                         stream);
 }
 
 cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *slot_of,

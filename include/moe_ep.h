@@ -166,6 +166,43 @@ MOE_API moe_status moe_combine(int T, int H, int k, const void *y, const int32_t
                        cudaStream_t stream);
 
 /*
+ * moe_combine_backward -- gradient of moe_combine (the backward Dispatch).
+ *
+ * HyperParallel-MoE, section 2.2 / Figure 2(b): the backward Dispatch is the
+ * gradient of the forward Combine.  With out[t] = sum_j w[t,j] * y[slot_of[t,j]]:
+ *
+ *   dout     [T, H]    bf16 gradient of out
+ *   y        [T*k, H]  bf16 forward expert outputs (receive order); may be NULL
+ *                      when dw is NULL
+ *   dy       [T*k, H]  out: bf16, dy[slot_of[t,j]] = w[t,j] * dout[t] (one fp32
+ *                      multiply, rounded once to bf16)
+ *   dw       [T, k]    out (may be NULL): fp32 <y[slot_of[t,j]], dout[t]>; the
+ *                      bf16 products are exact in fp32, the sum is accumulated
+ *                      in fp32 in a fixed order (deterministic; within
+ *                      (H-1) * 2^-24 * sum|y * dout| of the exact value)
+ *
+ * 1 <= k <= 32; H % 8 == 0.
+ */
+MOE_API moe_status moe_combine_backward(int T, int H, int k, const void *dout, const void *y,
+                                const int32_t *slot_of, const float *topk_w, void *dy,
+                                float *dw, uint32_t *err_word, cudaStream_t stream);
+
+/*
+ * moe_dispatch_backward -- gradient of moe_dispatch (the backward Combine).
+ *
+ * HyperParallel-MoE, section 2.2 / Figure 2(b): the backward Combine returns
+ * the input-activation gradient.  dx[t] = sum_j drecv[slot_of[t,j]]: fp32
+ * accumulation from +0 in slot order, rounded once to bf16 (MOE_OUT_BF16) or
+ * kept fp32 (MOE_OUT_F32) -- moe_combine with unit weights.
+ *
+ *   drecv    [T*k, H]  bf16 gradient of recv
+ *   dx       [T, H]    out
+ */
+MOE_API moe_status moe_dispatch_backward(int T, int H, int k, const void *drecv,
+                                 const int32_t *slot_of, void *dx, int out_dtype,
+                                 uint32_t *err_word, cudaStream_t stream);
+
+/*
  * moe_dispatch_combine_flagged -- dispatch, an identity expert and combine in
  * one persistent kernel, with Data-as-Flag readiness instead of a barrier.
  *

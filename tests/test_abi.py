@@ -104,3 +104,8 @@ def test_payload_calls_reject_bad_shapes_and_alignment(m):
     assert L.moe_dispatch_combine_flagged(4, 64, 40, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 10,
                                           -1, None, None) == m.MOE_ERR_UNSUPPORTED
     assert m.moe_flag_words(1024, 7168, 8) == 1024 * 8 * 7
+    # backward: k above 32, dw without y, bad output dtype
+    assert L.moe_combine_backward(4, 64, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                  None) == m.MOE_ERR_UNSUPPORTED
+    assert L.moe_combine_backward(4, 64, 2, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None) == bad
+    assert L.moe_dispatch_backward(4, 64, 2, FAKE, FAKE, FAKE, 3, None, None) == bad
