@@ -516,12 +516,151 @@ static cudaError_t launch_combine_backward_t(int T, int H, int k, const void *do
                       slot_of, topk_w, static_cast<uint4 *>(dy), dw, T, k, H / 8, err_word);
 }
 
+// Small k (<= 4): too little work per token for a whole CTA.  The same
+// arithmetic with WPT warps per token (here 1: each warp owns a token) and two
+// vectors per iteration, so that a warp keeps 2 * (1 + k) loads in flight; the
+// token's dot products are reduced by its warp's xor tree, then (when WPT > 1)
+// by its warps in index order.
+template <int KMAX, int UC, int MINB>
+__global__ void __launch_bounds__(32 * CB_WARPS, MINB)
+    combine_backward_warp_kernel(const uint4 *__restrict__ dout, const uint4 *__restrict__ y,
+                            const int32_t *__restrict__ slot_of, const float *__restrict__ topk_w,
+                            uint4 *__restrict__ dy, float *__restrict__ dw, int T, int k, int C,
+                            int wpt, uint32_t *err_word)
+{
+    __shared__ float red[CB_WARPS][KMAX];
+    wait_prior_grid();
+    allow_next_grid();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int N = T * k;
+    const int tpc = CB_WARPS / wpt;              // tokens per CTA pass
+    const int slice = warp % wpt;
+    const int per = (C + wpt - 1) / wpt;
+    const int c0 = slice * per, c1 = min(C, c0 + per);
+    const int64_t groups = ((int64_t)T + tpc - 1) / tpc;
+    for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {
+        const int64_t t = g * tpc + warp / wpt;
+        const bool tok = t < T;                  // warp-uniform
+        const int32_t ms = tok && lane < k ? ld_nc_s32(slot_of + t * k + lane) : -1;
+        const float mw = tok && lane < k ? ld_nc_f32(topk_w + t * k + lane) : 0.0f;
+        const unsigned okmask = __ballot_sync(FULL_MASK, lane < k && (unsigned)ms < (unsigned)N);
+        if (tok && slice == 0 && lane == 0 &&
+            okmask != (k >= 32 ? FULL_MASK : ((1u << k) - 1u)))
+            report(err_word, MOE_ERRBIT_BAD_INDEX);
+        float part[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            part[j] = 0.0f;
+        // warp-uniform loop (the shuffles below need every lane); a lane past
+        // the slice only skips its loads, arithmetic and stores
+        for (int cb = c0; tok && cb < c1; cb += 32 * UC) {
+            bool act[UC];
+            float df[UC][8];
+#pragma unroll
+            for (int u = 0; u < UC; ++u) {
+                const int c = cb + 32 * u + lane;
+                act[u] = c < c1;
+                const uint4 d = act[u] ? ld_stream_v4(dout + t * C + c) : make_uint4(0, 0, 0, 0);
+                const uint32_t d4[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    df[u][2 * h] = bf16lo(d4[h]);
+                    df[u][2 * h + 1] = bf16hi(d4[h]);
+                }
+            }
+#pragma unroll
+            for (int jb = 0; jb < KMAX; jb += 8) {
+                if (jb >= k)
+                    break;
+                uint4 yv[8][UC];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = jb + q;
+                    const int32_t s = __shfl_sync(FULL_MASK, ms, j & 31);
+                    const bool okj = y && j < k && ((okmask >> j) & 1u);
+#pragma unroll
+                    for (int u = 0; u < UC; ++u)
+                        yv[q][u] = (okj && act[u])
+                                       ? ld_stream_v4(y + (int64_t)s * C + cb + 32 * u + lane)
+                                       : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = jb + q;
+                    const int32_t s = __shfl_sync(FULL_MASK, ms, j & 31);
+                    const float w = __shfl_sync(FULL_MASK, mw, j & 31);
+                    if (j >= k || !((okmask >> j) & 1u))
+                        continue;
+#pragma unroll
+                    for (int u = 0; u < UC; ++u) {
+                        if (!act[u])
+                            continue;
+                        const uint32_t yw[4] = {yv[q][u].x, yv[q][u].y, yv[q][u].z, yv[q][u].w};
+                        uint32_t r[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            part[j] = __fmaf_rn(bf16lo(yw[h]), df[u][2 * h], part[j]);
+                            part[j] = __fmaf_rn(bf16hi(yw[h]), df[u][2 * h + 1], part[j]);
+                            const __nv_bfloat162 bb = __floats2bfloat162_rn(
+                                __fmul_rn(w, df[u][2 * h]), __fmul_rn(w, df[u][2 * h + 1]));
+                            r[h] = *reinterpret_cast<const uint32_t *>(&bb);
+                        }
+                        st_v4(dy + (int64_t)s * C + cb + 32 * u + lane, make_uint4(r[0], r[1], r[2], r[3]));
+                    }
+                }
+            }
+        }
+        if (dw) {
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                float v = part[j];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1)
+                    v += __shfl_xor_sync(FULL_MASK, v, o);
+                if (lane == 0)
+                    red[warp][j] = v;
+            }
+            __syncthreads();
+            if (tok && slice == 0 && lane < k) {
+                float v = 0.0f;
+                for (int i = 0; i < wpt; ++i)
+                    v += red[warp + i][lane];
+                dw[t * k + lane] = v;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <int KMAX, int UC, int MINB>
+static cudaError_t launch_combine_backward_warp(int T, int H, int k, const void *dout, const void *y,
+                                                const int32_t *slot_of, const float *topk_w,
+                                                void *dy, float *dw, uint32_t *err_word,
+                                                cudaStream_t stream)
+{
+    auto kern = combine_backward_warp_kernel<KMAX, UC, MINB>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * CB_WARPS, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t groups = ((int64_t)T + CB_WARPS - 1) / CB_WARPS;  // one warp per token
+    const int64_t cap = (int64_t)sm_count() * per_sm * 4;
+    const int64_t g = groups < cap ? groups : cap;
+    return launch_pdl(kern, dim3((unsigned)g), dim3(32 * CB_WARPS), 0, stream,
+                      static_cast<const uint4 *>(dout), static_cast<const uint4 *>(y), slot_of,
+                      topk_w, static_cast<uint4 *>(dy), dw, T, k, H / 8, 1, err_word);
+}
+
 cudaError_t launch_combine_backward(int T, int H, int k, const void *dout, const void *y,
                                     const int32_t *slot_of, const float *topk_w, void *dy,
                                     float *dw, uint32_t *err_word, cudaStream_t stream)
 {
     if (T == 0)
         return cudaSuccess;
+    if (k <= 4)
+        return launch_combine_backward_warp<8, 2, 2>(T, H, k, dout, y, slot_of, topk_w, dy, dw,
+                                                     err_word, stream);
     if (k <= 8)
         return launch_combine_backward_t<8>(T, H, k, dout, y, slot_of, topk_w, dy, dw, err_word,
                                             stream);
