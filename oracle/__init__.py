@@ -55,9 +55,12 @@ def _bind(path: str) -> ctypes.CDLL:
     L.oracle_f32_to_bf16_array.restype = None
     L.oracle_combine_backward.argtypes = [I, I, I, P, P, P, P, P, P, P]
     L.oracle_dispatch_backward.argtypes = [I, I, I, P, P, P, I]
+    L.oracle_layout_coalesced.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
+    L.oracle_dispatch_coalesced.argtypes = [I, I, I, P, P, P]
     for f in ("oracle_layout", "oracle_dispatch", "oracle_dispatch_quant",
               "oracle_combine", "oracle_combine_f64", "oracle_abi_version",
-              "oracle_combine_backward", "oracle_dispatch_backward"):
+              "oracle_combine_backward", "oracle_dispatch_backward",
+              "oracle_layout_coalesced", "oracle_dispatch_coalesced"):
         getattr(L, f).restype = ctypes.c_int
     return L
 
@@ -197,6 +200,33 @@ def dispatch_backward(drecv_bf16: np.ndarray, slot_of: np.ndarray, out_dtype: st
     _check(lib().oracle_dispatch_backward(T, H, k, _p(dr), _p(so), _p(out),
                                           0 if out_dtype == "bf16" else 1))
     return out
+
+
+def layout_coalesced(topk_idx: np.ndarray, E: int, R: int, slot_of: np.ndarray):
+    """Returns (rank_counts_c[R], rank_offsets_c[R+1], crow[T,k], src_pair_c[Nc],
+    expand[T*k])."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    T, k = idx.shape
+    counts = np.empty(R, np.int32)
+    offs = np.empty(R + 1, np.int32)
+    crow = np.empty((T, k), np.int32)
+    src = np.full(T * k, -1, np.int32)
+    expand = np.empty(T * k, np.int32)
+    _check(lib().oracle_layout_coalesced(T, k, E, R, _p(idx), _p(so), _p(counts), _p(offs),
+                                         _p(crow), _p(src), _p(expand)))
+    return counts, offs, crow, src[: offs[-1]].copy(), expand
+
+
+def dispatch_coalesced(x_bf16: np.ndarray, crow: np.ndarray, n_rows: int) -> np.ndarray:
+    """recv_c[crow[t, j]] = x[t]; uint16 [n_rows, H]."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    cr = np.ascontiguousarray(crow, dtype=np.int32)
+    T, H = x.shape
+    k = cr.shape[1]
+    out = np.zeros((max(T * k, 1), H), np.uint16)
+    _check(lib().oracle_dispatch_coalesced(T, H, k, _p(x), _p(cr), _p(out)))
+    return out[:n_rows]
 
 
 def e4m3_encode(f: np.ndarray) -> np.ndarray:

@@ -24,6 +24,10 @@
  *                          bf16 rounding of fp32 products; numpy einsum for dw
  *   oracle_dispatch_backward oracle_combine with unit weights (special case),
  *                          float64 closed form within the fp32 bound
+ *   oracle_layout_coalesced  set-based brute force in numpy; invariants (row count
+ *                          = sum of distinct ranks per token, token order per rank,
+ *                          expand consistent with the plain slot map)
+ *   oracle_dispatch_coalesced rows equal the owning token's row
  */
 #include <float.h>
 #include <math.h>
@@ -386,6 +390,99 @@ int oracle_dispatch_backward(int T, int H, int k, const uint16_t *drecv, const i
                 ((uint16_t *)dx)[(int64_t)t * H + h] = oracle_f32_to_bf16(acc);
             else
                 ((float *)dx)[(int64_t)t * H + h] = acc;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Rank-coalesced layout and dispatch.  UBEP section 2.3: a token may go to   */
+/* several experts; RailWave section 3.1 (existing token coalescing): a token */
+/* needs to cross to a rank once, however many of its experts live there.     */
+/* Pair (t, j) "owns" (t, rank(e_tj)) when no earlier slot j' < j of token t  */
+/* chose an expert on the same rank.  Owners get one coalesced row each:      */
+/* rank-segmented, in token order inside a rank, no padding.                  */
+/*   crow[t,j]      coalesced row of (t, rank(e_tj)) (owners and the rest)    */
+/*   src_pair_c[c]  owner pair t*k+j of coalesced row c, for c < Nc           */
+/*   expand[s]      coalesced row holding the input of slot s of the plain    */
+/*                  layout: expand[slot_of[t,j]] = crow[t,j]                  */
+/* and the coalesced dispatch writes recv_c[c] = x[src_pair_c[c] / k].        */
+/* ------------------------------------------------------------------------- */
+int oracle_layout_coalesced(int T, int k, int E, int R, const int32_t *topk_idx,
+                            const int32_t *slot_of, int32_t *rank_counts_c,
+                            int32_t *rank_offsets_c, int32_t *crow, int32_t *src_pair_c,
+                            int32_t *expand)
+{
+    if (T < 0 || k < 1 || E < 1 || R < 1 || E % R != 0)
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    const int El = E / R;
+    for (int64_t i = 0; i < N; ++i)
+        if (topk_idx[i] < 0 || topk_idx[i] >= E)
+            return ORACLE_ERR_BAD_INDEX;
+    for (int r = 0; r < R; ++r)
+        rank_counts_c[r] = 0;
+    /* 1. owners and their count per rank */
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            const int r = topk_idx[(int64_t)t * k + j] / El;
+            int owner = 1;
+            for (int jj = 0; jj < j; ++jj)
+                if (topk_idx[(int64_t)t * k + jj] / El == r)
+                    owner = 0;
+            if (owner)
+                rank_counts_c[r] += 1;
+        }
+    }
+    /* 2. exclusive scan over ranks */
+    rank_offsets_c[0] = 0;
+    for (int r = 0; r < R; ++r)
+        rank_offsets_c[r + 1] = rank_offsets_c[r] + rank_counts_c[r];
+    /* 3. owners take rows in token order; the other slots share their owner's */
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)R);
+    if (!cursor)
+        return ORACLE_ERR_INVALID_ARG;
+    for (int r = 0; r < R; ++r)
+        cursor[r] = rank_offsets_c[r];
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            const int64_t i = (int64_t)t * k + j;
+            const int r = topk_idx[i] / El;
+            int owner_j = j;
+            for (int jj = j - 1; jj >= 0; --jj)
+                if (topk_idx[(int64_t)t * k + jj] / El == r)
+                    owner_j = jj;
+            if (owner_j == j) {
+                const int32_t c = cursor[r]++;
+                crow[i] = c;
+                src_pair_c[c] = (int32_t)i;
+            } else {
+                crow[i] = crow[(int64_t)t * k + owner_j];
+            }
+        }
+    }
+    free(cursor);
+    for (int64_t i = 0; i < N; ++i) {
+        const int32_t s = slot_of[i];
+        if (s < 0 || s >= N)
+            return ORACLE_ERR_BAD_INDEX;
+        expand[s] = crow[i];
+    }
+    return ORACLE_OK;
+}
+
+int oracle_dispatch_coalesced(int T, int H, int k, const uint16_t *x, const int32_t *crow,
+                              uint16_t *recv_c)
+{
+    if (T < 0 || H < 1 || k < 1)
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            const int32_t c = crow[(int64_t)t * k + j];
+            if (c < 0 || c >= N)
+                return ORACLE_ERR_BAD_INDEX;
+            memcpy(recv_c + (int64_t)c * H, x + (int64_t)t * H, sizeof(uint16_t) * (size_t)H);
         }
     }
     return ORACLE_OK;

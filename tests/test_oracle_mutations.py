@@ -11,6 +11,7 @@ import test_oracle_dispatch as td
 import test_oracle_layout as tl
 import test_oracle_bf16 as tb
 import test_oracle_backward as tbw
+import test_oracle_coalesced as tco
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "moe_oracle.c")
@@ -40,6 +41,9 @@ MUTANTS = {
     # backward: dx skips the last slot
     "dx_drop": ("            for (int j = 0; j < k; ++j)\n                acc = acc + bf16_to_f32(",
                 "            for (int j = 0; j + 1 < k; ++j)\n                acc = acc + bf16_to_f32("),
+    # coalesced: owner taken as the last matching slot instead of the first
+    "coalesced_owner": ("            for (int jj = j - 1; jj >= 0; --jj)\n                if (topk_idx[(int64_t)t * k + jj] / El == r)\n                    owner_j = jj;",
+                        "            for (int jj = 0; jj < j; ++jj)\n                if (topk_idx[(int64_t)t * k + jj] / El == r)\n                    owner_j = jj;"),
     # bf16: ties rounded up instead of to even
     "bf16_ties": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (lower >= 0x8000u)"),
 }
@@ -61,7 +65,9 @@ def _pins():
              lambda: tc.test_bf16_output_is_rounded_fp32_output("fuzz0", None),
              tb.test_random_and_special_values_match_torch,
              lambda: tbw.test_combine_backward_matches_autograd(tbw.CASES[1]),
-             lambda: tbw.test_dispatch_backward_is_unit_weight_combine(tbw.CASES[1])]
+             lambda: tbw.test_dispatch_backward_is_unit_weight_combine(tbw.CASES[1]),
+             tco.test_coalesced_hand_worked,
+             lambda: tco.test_coalesced_layout_matches_brute_force(*tco.CASES[7])]
     return pins
 
 
