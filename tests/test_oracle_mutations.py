@@ -41,9 +41,9 @@ MUTANTS = {
     # backward: dx skips the last slot
     "dx_drop": ("            for (int j = 0; j < k; ++j)\n                acc = acc + bf16_to_f32(",
                 "            for (int j = 0; j + 1 < k; ++j)\n                acc = acc + bf16_to_f32("),
-    # coalesced: owner taken as the last matching slot instead of the first
-    "coalesced_owner": ("            for (int jj = j - 1; jj >= 0; --jj)\n                if (topk_idx[(int64_t)t * k + jj] / El == r)\n                    owner_j = jj;",
-                        "            for (int jj = 0; jj < j; ++jj)\n                if (topk_idx[(int64_t)t * k + jj] / El == r)\n                    owner_j = jj;"),
+    # coalesced: tokens coalesced per expert instead of per rank
+    "coalesced_key": ("            for (int jj = j - 1; jj >= 0; --jj)\n                if (topk_idx[(int64_t)t * k + jj] / El == r)\n                    owner_j = jj;",
+                      "            for (int jj = j - 1; jj >= 0; --jj)\n                if (topk_idx[(int64_t)t * k + jj] == topk_idx[i])\n                    owner_j = jj;"),
     # bf16: ties rounded up instead of to even
     "bf16_ties": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (lower >= 0x8000u)"),
 }
