@@ -39,6 +39,9 @@ SIGNATURES = {
     "moe_flag_words": ([_I, _I, _I], ctypes.c_size_t),
     "moe_combine_backward": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_dispatch_backward": ([_I, _I, _I, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
+    "moe_layout_coalesced": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P],
+                             ctypes.c_int),
+    "moe_dispatch_coalesced": ([_I, _I, _I, _P, _P, _I, _P, _U32P, _P], ctypes.c_int),
     "moe_dispatch_combine_flagged": ([_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_uint32,
                                       ctypes.c_uint64, ctypes.c_int64, _U32P, _P], ctypes.c_int),
 }
@@ -162,6 +165,64 @@ def moe_layout_noalloc(topk_idx: torch.Tensor, E: int, R: int, *, out: Layout,
                                    _ptr(out.slot_of), _ptr(out.src_of), _ptr(err_word),
                                    _stream(stream)), "moe_layout_noalloc")
     return out
+
+
+class CoalescedLayout(NamedTuple):
+    rank_counts_c: torch.Tensor   # int32 [R]
+    rank_offsets_c: torch.Tensor  # int32 [R+1]; [R] = Nc
+    crow: torch.Tensor            # int32 [T, k]
+    src_pair_c: torch.Tensor      # int32 [T*k]; first Nc entries written
+    expand: torch.Tensor          # int32 [T*k]
+
+
+def moe_layout_coalesced(topk_idx: torch.Tensor, slot_of: torch.Tensor, E: int, R: int, *,
+                         workspace: Optional[torch.Tensor] = None,
+                         err_word: Optional[torch.Tensor] = None,
+                         out: Optional[CoalescedLayout] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> CoalescedLayout:
+    """One row per (token, distinct destination rank); expand maps plain slots
+    to those rows (see moe_ep.h)."""
+    if topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be [T, k]")
+    T, k = topk_idx.shape
+    _want(topk_idx, "topk_idx", torch.int32)
+    _want(slot_of, "slot_of", torch.int32, (T, k))
+    dev = topk_idx.device
+    if out is None:
+        out = CoalescedLayout(torch.empty(R, dtype=torch.int32, device=dev),
+                              torch.empty(R + 1, dtype=torch.int32, device=dev),
+                              torch.empty((T, k), dtype=torch.int32, device=dev),
+                              torch.empty(T * k, dtype=torch.int32, device=dev),
+                              torch.empty(T * k, dtype=torch.int32, device=dev))
+    need = moe_layout_workspace_bytes(T, k, R)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    _check(_lib.moe_layout_coalesced(T, k, E, R, _ptr(topk_idx), _ptr(slot_of),
+                                     _ptr(out.rank_counts_c), _ptr(out.rank_offsets_c),
+                                     _ptr(out.crow), _ptr(out.src_pair_c), _ptr(out.expand),
+                                     _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _ptr(err_word), _stream(stream)), "moe_layout_coalesced")
+    return out
+
+
+def moe_dispatch_coalesced(x: torch.Tensor, crow: torch.Tensor, rows: int, *,
+                           recv_c: Optional[torch.Tensor] = None,
+                           err_word: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """recv_c[crow[t, j]] = x[t], each coalesced row written once; `rows` is
+    recv_c's capacity (at least Nc; T * min(k, R) always suffices)."""
+    T, H = x.shape
+    k = crow.shape[1]
+    _want(x, "x", torch.bfloat16)
+    _want(crow, "crow", torch.int32, (T, k))
+    if recv_c is None:
+        recv_c = torch.empty((rows, H), dtype=torch.bfloat16, device=x.device)
+    elif recv_c.shape[0] < rows:
+        raise ValueError("recv_c has fewer than `rows` rows")
+    _check(_lib.moe_dispatch_coalesced(T, H, k, _ptr(x), _ptr(crow), rows, _ptr(recv_c),
+                                       _ptr(err_word), _stream(stream)), "moe_dispatch_coalesced")
+    return recv_c
 
 
 def moe_dispatch(x: torch.Tensor, slot_of: torch.Tensor, *, recv: Optional[torch.Tensor] = None,
@@ -332,5 +393,6 @@ __all__ = [
     "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
     "moe_combine", "moe_read_error", "moe_flag_words", "FlagWords",
     "moe_combine_backward", "moe_dispatch_backward",
+    "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced",
     "moe_dispatch_combine_flagged", "LIB_PATH", "SIGNATURES",
 ]

@@ -121,6 +121,47 @@ moe_status moe_dispatch(int T, int H, int k, const void *x, const int32_t *slot_
     return from_cuda(moe::launch_dispatch_bf16(T, H, k, x, slot_of, recv, err_word, stream));
 }
 
+moe_status moe_layout_coalesced(int T, int k, int E, int R, const int32_t *topk_idx,
+                                const int32_t *slot_of, int32_t *rank_counts_c,
+                                int32_t *rank_offsets_c, int32_t *crow, int32_t *src_pair_c,
+                                int32_t *expand, void *workspace, size_t workspace_bytes,
+                                uint32_t *err_word, cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || E < 1 || R < 1 || E % R != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (E > MOE_MAX_EXPERTS)
+        return MOE_ERR_UNSUPPORTED;
+    if (!rank_counts_c || !rank_offsets_c)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !slot_of || !crow || !src_pair_c || !expand || !workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 4) || !aligned(slot_of, 4) || !aligned(rank_counts_c, 4) ||
+        !aligned(rank_offsets_c, 4) || !aligned(crow, 4) || !aligned(src_pair_c, 4) ||
+        !aligned(expand, 4) || !aligned(workspace, 16) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && workspace_bytes < moe::layout_workspace_bytes((int64_t)T * k, R))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_layout_coalesced(T, k, E, R, topk_idx, slot_of, rank_counts_c,
+                                                  rank_offsets_c, crow, src_pair_c, expand,
+                                                  workspace, err_word, stream));
+}
+
+moe_status moe_dispatch_coalesced(int T, int H, int k, const void *x, const int32_t *crow,
+                                  int rows, void *recv_c, uint32_t *err_word,
+                                  cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0 || rows < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (k > 32)
+        return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !crow || !recv_c))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv_c, 16) || !aligned(crow, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_dispatch_coalesced(T, H, k, x, crow, recv_c, rows, err_word,
+                                                    stream));
+}
+
 moe_status moe_dispatch_quant(int T, int H, int k, const void *x, const int32_t *slot_of,
                               uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
                               cudaStream_t stream)

@@ -41,17 +41,22 @@ static_assert(DB_STAGES >= 2 && DB_STAGES <= 16, "stage ring size");
 // from it have finished reading shared memory (bulk async-group accounting:
 // every lane commits one group per unit, possibly empty).  The row is read
 // from HBM once and written k times with no per-element instructions.
+//
+// COAL: rows go to the rank-coalesced buffer (one row per token and distinct
+// destination rank).  slot_of is then the coalesced row map, where every slot
+// of a token on one rank names the same row; only the lowest such slot
+// stores it, so each row is written once.  `rows` bounds the row indices.
+template <bool COAL>
 __global__ void __launch_bounds__(32)
     dispatch_bulk_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ slot_of,
                          uint8_t *__restrict__ recv, int T, int k, int64_t rowbytes, int CH,
-                         int nchunks, int64_t units, uint32_t *err_word)
+                         int nchunks, int64_t units, int rows, uint32_t *err_word)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t bars = smem_addr(smem);
     const uint32_t stages = bars + 128;
     auto full = [&](int s) { return bars + 8u * s; };
     const int lane = threadIdx.x;
-    const int N = T * k;
 
     if (lane == 0) {
         for (int s = 0; s < DB_STAGES; ++s)
@@ -92,8 +97,18 @@ __global__ void __launch_bounds__(32)
     int64_t t = u0 / nchunks;
     int c = (int)(u0 - t * nchunks);
     const bool kl = lane < k;
+    // a lane stores its slot's row unless (COAL) a lower slot of the token
+    // names the same row
+    const unsigned kmask = k >= 32 ? FULL_MASK : (1u << k) - 1u;
+    auto first_of_row = [&](int32_t v) {
+        if (!COAL)
+            return kl;
+        const unsigned same = __match_any_sync(FULL_MASK, v) & kmask;
+        return kl && (same & lanemask_lt()) == 0;
+    };
     int32_t cur = kl ? ld_nc_s32(slot_of + t * k + lane) : 0;
     int32_t nxt = kl && t + 1 < T ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+    bool st = first_of_row(cur);
     int64_t n = 0;
     bool timed_out = false;
     for (; n < nloc; ++n) {
@@ -102,6 +117,7 @@ __global__ void __launch_bounds__(32)
             ++t;
             cur = nxt;
             nxt = kl && t + 1 < T ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+            st = first_of_row(cur);
         }
         const int s = (int)(n % DB_STAGES);
         if (!mbar_wait(full(s), (uint32_t)(n / DB_STAGES) & 1)) {
@@ -110,8 +126,8 @@ __global__ void __launch_bounds__(32)
         }
         const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
         fence_proxy_async_smem();
-        if (kl) {
-            if ((unsigned)cur < (unsigned)N)
+        if (st) {
+            if ((unsigned)cur < (unsigned)rows)
                 bulk_s2g(recv + (int64_t)cur * rowbytes + (int64_t)c * CH, stages + (uint32_t)s * CH, cb);
             else if (c == 0)
                 report(err_word, MOE_ERRBIT_BAD_INDEX);
@@ -283,34 +299,50 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
     }
 }
 
+template <bool COAL>
+static cudaError_t launch_dispatch_bulk(int T, int H, int k, const void *x,
+                                       const int32_t *slot_of, void *recv, int rows,
+                                       uint32_t *err_word, cudaStream_t stream)
+{
+    const int64_t rowbytes = 2 * (int64_t)H;
+    const int CH = rowbytes < DB_CHUNK ? (int)rowbytes : DB_CHUNK;
+    const int nchunks = (int)((rowbytes + CH - 1) / CH);
+    const int64_t units = (int64_t)T * nchunks;
+    const size_t smem = 128 + (size_t)DB_STAGES * CH;
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024)
+        e = cudaFuncSetAttribute(dispatch_bulk_kernel<COAL>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bulk_kernel<COAL>, 32,
+                                                      smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t g = units < cap ? units : cap;
+    return launch_pdl(dispatch_bulk_kernel<COAL>, dim3((unsigned)g), dim3(32), smem, stream,
+                      static_cast<const uint8_t *>(x), slot_of, static_cast<uint8_t *>(recv), T, k,
+                      rowbytes, CH, nchunks, units, rows, err_word);
+}
+
+cudaError_t launch_dispatch_coalesced(int T, int H, int k, const void *x, const int32_t *crow,
+                                      void *recv_c, int rows, uint32_t *err_word,
+                                      cudaStream_t stream)
+{
+    if (T == 0)
+        return cudaSuccess;
+    return launch_dispatch_bulk<true>(T, H, k, x, crow, recv_c, rows, err_word, stream);
+}
+
 cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32_t *slot_of,
                                  void *recv, uint32_t *err_word, cudaStream_t stream)
 {
     if (T == 0)
         return cudaSuccess;
-    if (k <= 32) {
-        const int64_t rowbytes = 2 * (int64_t)H;
-        const int CH = rowbytes < DB_CHUNK ? (int)rowbytes : DB_CHUNK;
-        const int nchunks = (int)((rowbytes + CH - 1) / CH);
-        const int64_t units = (int64_t)T * nchunks;
-        const size_t smem = 128 + (size_t)DB_STAGES * CH;
-        cudaError_t e = cudaSuccess;
-        if (smem > 48 * 1024)
-            e = cudaFuncSetAttribute(dispatch_bulk_kernel,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        int per_sm = 1;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bulk_kernel, 32, smem) !=
-                cudaSuccess ||
-            per_sm < 1)
-            per_sm = 1;
-        const int64_t cap = (int64_t)sm_count() * per_sm;
-        const int64_t g = units < cap ? units : cap;
-        return launch_pdl(dispatch_bulk_kernel, dim3((unsigned)g), dim3(32), smem, stream,
-                          static_cast<const uint8_t *>(x), slot_of, static_cast<uint8_t *>(recv), T,
-                          k, rowbytes, CH, nchunks, units, err_word);
-    }
+    if (k <= 32)
+        return launch_dispatch_bulk<false>(T, H, k, x, slot_of, recv, T * k, err_word, stream);
     const int C = H / 8;
     const int groups = (C + 32 * DISPATCH_U - 1) / (32 * DISPATCH_U);
     const int64_t items = (int64_t)T * groups;

@@ -15,6 +15,16 @@ cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
                           int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
                           void *workspace, uint32_t *err_word, cudaStream_t stream);
 
+cudaError_t launch_layout_coalesced(int T, int k, int E, int R, const int32_t *topk_idx,
+                                    const int32_t *slot_of, int32_t *rank_counts_c,
+                                    int32_t *rank_offsets_c, int32_t *crow, int32_t *src_pair_c,
+                                    int32_t *expand, void *workspace, uint32_t *err_word,
+                                    cudaStream_t stream);
+
+cudaError_t launch_dispatch_coalesced(int T, int H, int k, const void *x, const int32_t *crow,
+                                      void *recv_c, int rows, uint32_t *err_word,
+                                      cudaStream_t stream);
+
 cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32_t *slot_of,
                                  void *recv, uint32_t *err_word, cudaStream_t stream);
 

@@ -41,22 +41,39 @@ constexpr size_t LAYOUT_BARRIER_BYTES = 256;  // workspace head: grid-barrier co
 constexpr int NO_PAIR = -1;
 constexpr int BAD_PAIR = -2;
 
-// Loads the expert ids of up to LAYOUT_BATCH warp steps starting at pair
-// `first` (lane-strided), marking pairs at or past `end` as NO_PAIR.
+// Key of pair i: its expert id, or (COAL) its destination rank when it is the
+// first slot of its token that chose that rank, else NO_PAIR (it takes no
+// row).  Ids outside [0, E) give BAD_PAIR.
+template <bool COAL>
+__device__ __forceinline__ int pair_key(const int32_t *__restrict__ idx, int64_t i, int E, int El,
+                                        int k)
+{
+    const int e = ld_nc_s32(idx + i);
+    if ((unsigned)e >= (unsigned)E)
+        return BAD_PAIR;
+    if (!COAL)
+        return e;
+    const int r = e / El;
+    const int j = (int)(i % k);
+    for (int jj = 0; jj < j; ++jj) {
+        const int e2 = ld_nc_s32(idx + i - j + jj);
+        if ((unsigned)e2 < (unsigned)E && e2 / El == r)
+            return NO_PAIR;
+    }
+    return r;
+}
+
+// Loads the keys of up to LAYOUT_BATCH warp steps starting at pair `first`
+// (lane-strided), marking pairs at or past `end` as NO_PAIR.
+template <bool COAL>
 __device__ __forceinline__ void load_batch(const int32_t *__restrict__ idx, int64_t first,
-                                           int64_t end, int E, int lane,
+                                           int64_t end, int E, int El, int k, int lane,
                                            int (&ev)[LAYOUT_BATCH])
 {
 #pragma unroll
     for (int b = 0; b < LAYOUT_BATCH; ++b) {
         const int64_t i = first + b * 32 + lane;
-        int e = NO_PAIR;
-        if (i < end) {
-            e = ld_nc_s32(idx + i);
-            if ((unsigned)e >= (unsigned)E)
-                e = BAD_PAIR;
-        }
-        ev[b] = e;
+        ev[b] = i < end ? pair_key<COAL>(idx, i, E, El, k) : NO_PAIR;
     }
 }
 
@@ -139,9 +156,12 @@ __device__ bool grid_barrier(unsigned *bar, uint32_t *err_word)
     } while (0)
 #endif
 
-template <int NBITS>
+// Keys: expert ids (K = E), or with COAL destination ranks of owner pairs
+// (K = R); e_real and El are the expert count and experts per rank.
+template <int NBITS, bool COAL>
 __global__ void __launch_bounds__(LAYOUT_THREADS)
-    layout_kernel(const int32_t *__restrict__ idx, int64_t N, int E, int R, int span,
+    layout_kernel(const int32_t *__restrict__ idx, int64_t N, int E, int R, int e_real, int El,
+                  int k, int span,
                   int tiles, unsigned *barrier, int32_t *tile_counts,
                   int32_t *__restrict__ expert_counts, int32_t *__restrict__ expert_offsets,
                   int32_t *__restrict__ rank_offsets, int32_t *__restrict__ slot_of,
@@ -173,7 +193,7 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
     bool bad = false;
     for (int64_t first = begin; first < end; first += 32 * LAYOUT_BATCH) {
         int ev[LAYOUT_BATCH];
-        load_batch(idx, first, end, E, lane, ev);
+        load_batch<COAL>(idx, first, end, e_real, El, k, lane, ev);
 #pragma unroll
         for (int b = 0; b < LAYOUT_BATCH; ++b) {
             bad |= ev[b] == BAD_PAIR;
@@ -260,9 +280,11 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
     __syncthreads();
     const int32_t total = carry[0];
     if (blockIdx.x == 0) {
-        const int El = E / R;
-        for (int r = tid; r <= R; r += LAYOUT_THREADS)
-            rank_offsets[r] = r == R ? total : offs[r * El];
+        if (rank_offsets) {
+            const int Kl = E / R;
+            for (int r = tid; r <= R; r += LAYOUT_THREADS)
+                rank_offsets[r] = r == R ? total : offs[r * Kl];
+        }
         if (tid == 0)
             expert_offsets[E] = total;
     }
@@ -291,7 +313,7 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
             for (int b = 0; b < LAYOUT_BATCH; ++b)
                 ev[b] = ev0[b];
         } else {
-            load_batch(idx, first, end, E, lane, ev);
+            load_batch<COAL>(idx, first, end, e_real, El, k, lane, ev);
         }
 #pragma unroll
         for (int b = 0; b < LAYOUT_BATCH; ++b) {
@@ -353,8 +375,9 @@ size_t layout_workspace_bytes(int64_t N, int E)
     return LAYOUT_BARRIER_BYTES + bytes;
 }
 
-template <int NBITS>
-static cudaError_t launch_layout_t(int64_t N, int E, int R, const LayoutPlan &p,
+template <int NBITS, bool COAL>
+static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, int k,
+                                   const LayoutPlan &p,
                                    const int32_t *topk_idx, unsigned *barrier,
                                    int32_t *tile_counts, int32_t *expert_counts,
                                    int32_t *expert_offsets, int32_t *rank_offsets,
@@ -364,8 +387,8 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, const LayoutPlan &p,
     const size_t smem = layout_smem(E);
     cudaError_t e = cudaSuccess;
     if (smem > 48 * 1024)
-        e = cudaFuncSetAttribute(layout_kernel<NBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+        e = cudaFuncSetAttribute(layout_kernel<NBITS, COAL>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     // Cooperative: all CTAs are co-resident, as the grid barrier requires.
@@ -383,47 +406,50 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, const LayoutPlan &p,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS>, topk_idx, N, E, R, p.span, p.tiles, barrier,
-                           tile_counts, expert_counts, expert_offsets, rank_offsets, slot_of,
-                           src_of, err_word);
+    e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS, COAL>, topk_idx, N, E, R, e_real, El, k,
+                           p.span, p.tiles, barrier, tile_counts, expert_counts, expert_offsets,
+                           rank_offsets, slot_of, src_of, err_word);
     if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
         // the driver refused the attribute pair: launch cooperatively only
         (void)cudaGetLastError();
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS>, topk_idx, N, E, R, p.span, p.tiles,
-                               barrier, tile_counts, expert_counts, expert_offsets, rank_offsets,
-                               slot_of, src_of, err_word);
+        e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS, COAL>, topk_idx, N, E, R, e_real, El, k,
+                               p.span, p.tiles, barrier, tile_counts, expert_counts,
+                               expert_offsets, rank_offsets, slot_of, src_of, err_word);
     }
     return e;
 }
 
-cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
-                          int32_t *expert_counts, int32_t *expert_offsets,
-                          int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
-                          void *workspace, uint32_t *err_word, cudaStream_t stream)
+// Count / scan / slot map over keys in [0, K): expert ids (COAL false) or the
+// destination ranks of owner pairs (COAL true).
+template <bool COAL>
+static cudaError_t launch_keys(int T, int k, int K, int R, int e_real, int El,
+                               const int32_t *topk_idx, int32_t *counts, int32_t *offsets,
+                               int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
+                               void *workspace, uint32_t *err_word, cudaStream_t stream)
 {
     const int64_t N = (int64_t)T * k;
     if (N == 0) {
-        cudaError_t e = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, stream);
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * K, stream);
         if (e == cudaSuccess)
-            e = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), stream);
-        if (e == cudaSuccess)
+            e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (K + 1), stream);
+        if (e == cudaSuccess && rank_offsets)
             e = cudaMemsetAsync(rank_offsets, 0, sizeof(int32_t) * (R + 1), stream);
         return e;
     }
     const LayoutPlan p = layout_plan(N);
     int nbits = 0;
-    while ((1 << nbits) < E)
+    while ((1 << nbits) < K)
         ++nbits;
     unsigned *barrier = static_cast<unsigned *>(workspace);
     int32_t *tile_counts = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
                                                        LAYOUT_BARRIER_BYTES);
     switch (nbits) {
-#define MOE_LAYOUT_CASE(B)                                                                   \
-    case B:                                                                                  \
-        return launch_layout_t<B>(N, E, R, p, topk_idx, barrier, tile_counts, expert_counts, \
-                                  expert_offsets, rank_offsets, slot_of, src_of, err_word,   \
-                                  stream);
+#define MOE_LAYOUT_CASE(B)                                                                     \
+    case B:                                                                                    \
+        return launch_layout_t<B, COAL>(N, K, R, e_real, El, k, p, topk_idx, barrier,          \
+                                        tile_counts, counts, offsets, rank_offsets, slot_of,   \
+                                        src_of, err_word, stream);
         MOE_LAYOUT_CASE(0)
         MOE_LAYOUT_CASE(1)
         MOE_LAYOUT_CASE(2)
@@ -439,6 +465,68 @@ cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
     default:
         return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
+                          int32_t *expert_counts, int32_t *expert_offsets,
+                          int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
+                          void *workspace, uint32_t *err_word, cudaStream_t stream)
+{
+    return launch_keys<false>(T, k, E, R, E, E / R, topk_idx, expert_counts, expert_offsets,
+                              rank_offsets, slot_of, src_of, workspace, err_word, stream);
+}
+
+// Non-owner slots take their owner's coalesced row; expand[slot_of[i]] = crow[i].
+__global__ void coalesce_finish_kernel(const int32_t *__restrict__ idx,
+                                       const int32_t *__restrict__ slot_of, int32_t *crow,
+                                       int32_t *__restrict__ expand, int64_t N, int E, int El,
+                                       int k)
+{
+    wait_prior_grid();
+    allow_next_grid();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < N;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int e = ld_nc_s32(idx + i);
+        if ((unsigned)e >= (unsigned)E)
+            continue;
+        const int r = e / El;
+        const int j = (int)(i % k);
+        int owner = j;
+        for (int jj = 0; jj < j; ++jj) {
+            const int e2 = ld_nc_s32(idx + i - j + jj);
+            if ((unsigned)e2 < (unsigned)E && e2 / El == r) {
+                owner = jj;
+                break;
+            }
+        }
+        const int32_t c = owner == j ? crow[i] : crow[i - j + owner];
+        if (owner != j)
+            crow[i] = c;
+        const int32_t s = ld_nc_s32(slot_of + i);
+        if ((unsigned)s < (unsigned)N)
+            expand[s] = c;
+    }
+}
+
+cudaError_t launch_layout_coalesced(int T, int k, int E, int R, const int32_t *topk_idx,
+                                    const int32_t *slot_of, int32_t *rank_counts_c,
+                                    int32_t *rank_offsets_c, int32_t *crow, int32_t *src_pair_c,
+                                    int32_t *expand, void *workspace, uint32_t *err_word,
+                                    cudaStream_t stream)
+{
+    cudaError_t e = launch_keys<true>(T, k, R, R, E, E / R, topk_idx, rank_counts_c,
+                                      rank_offsets_c, nullptr, crow, src_pair_c, workspace,
+                                      err_word, stream);
+    const int64_t N = (int64_t)T * k;
+    if (e != cudaSuccess || N == 0)
+        return e;
+    const int threads = 256;
+    int64_t blocks = (N + threads - 1) / threads;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap)
+        blocks = cap;
+    return launch_pdl(coalesce_finish_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                      topk_idx, slot_of, crow, expand, N, E, E / R, k);
 }
 
 }  // namespace moe

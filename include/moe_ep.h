@@ -203,6 +203,60 @@ MOE_API moe_status moe_dispatch_backward(int T, int H, int k, const void *drecv,
                                  uint32_t *err_word, cudaStream_t stream);
 
 /*
+ * moe_layout_coalesced -- rank-coalesced row map: one receive row per token
+ * and distinct destination rank.
+ *
+ * RailWave, section 3.1 (token coalescing: a token crosses to a rank once,
+ * however many of its experts live there); UBEP, section 2.3 (a token goes to
+ * several experts).  Pair (t, j) owns (t, rank(e_tj)) when no earlier slot
+ * j' < j of token t chose an expert on the same rank (rank(e) = e / (E / R)).
+ * Owners take rows rank by rank, in token order inside a rank, no padding.
+ *
+ *   topk_idx       [T, k]  int32 expert ids in [0, E)
+ *   slot_of        [T, k]  int32 plain slot map from moe_layout (same topk_idx)
+ *   rank_counts_c  [R]     out: coalesced rows per destination rank
+ *   rank_offsets_c [R+1]   out: exclusive scan of rank_counts_c; [R] = Nc
+ *   crow           [T, k]  out: coalesced row of (t, rank(e_tj)), for owners and
+ *                          the other slots alike
+ *   src_pair_c     [T*k]   out: owner pair t*k+j of row c, for c < Nc (the
+ *                          rest is left unwritten)
+ *   expand         [T*k]   out: expand[slot_of[t,j]] = crow[t,j], the coalesced
+ *                          row that holds the input of each plain slot
+ *   workspace      moe_layout_workspace_bytes(T, k, R) bytes, zero-filled once
+ *                  (the same rules as moe_layout's; the two may not share one
+ *                  workspace concurrently)
+ *
+ * Ids outside [0, E) set MOE_ERRBIT_BAD_INDEX, get crow -1 and no row.
+ * 1 <= R <= E <= MOE_MAX_EXPERTS, E % R == 0.  Two launches: the row map over
+ * owners, then a pass that resolves the other slots and expand.
+ */
+MOE_API moe_status moe_layout_coalesced(int T, int k, int E, int R, const int32_t *topk_idx,
+                                const int32_t *slot_of, int32_t *rank_counts_c,
+                                int32_t *rank_offsets_c, int32_t *crow, int32_t *src_pair_c,
+                                int32_t *expand, void *workspace, size_t workspace_bytes,
+                                uint32_t *err_word, cudaStream_t stream);
+
+/*
+ * moe_dispatch_coalesced -- copy each token's row once per destination rank.
+ *
+ * RailWave, section 3.1 (coalesced dispatch sends one copy of a token per
+ * destination rank).  recv_c[crow[t, j]] = x[t]; each row is written once
+ * (by the lowest slot of the token that names it).
+ *
+ *   x       [T, H]     bf16 token rows (16-byte aligned)
+ *   crow    [T, k]     from moe_layout_coalesced
+ *   rows    capacity of recv_c in rows (rows named by crow must be below it;
+ *           Nc <= T * min(k, R))
+ *   recv_c  [rows, H]  out: bf16 (16-byte aligned)
+ *
+ * 1 <= k <= 32 (larger k: MOE_ERR_UNSUPPORTED); H % 8 == 0.  Row indices
+ * outside [0, rows) set MOE_ERRBIT_BAD_INDEX and are skipped.
+ */
+MOE_API moe_status moe_dispatch_coalesced(int T, int H, int k, const void *x,
+                                  const int32_t *crow, int rows, void *recv_c,
+                                  uint32_t *err_word, cudaStream_t stream);
+
+/*
  * moe_dispatch_combine_flagged -- dispatch, an identity expert and combine in
  * one persistent kernel, with Data-as-Flag readiness instead of a barrier.
  *

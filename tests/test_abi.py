@@ -109,3 +109,24 @@ def test_payload_calls_reject_bad_shapes_and_alignment(m):
                                   None) == m.MOE_ERR_UNSUPPORTED
     assert L.moe_combine_backward(4, 64, 2, FAKE, None, FAKE, FAKE, FAKE, FAKE, None, None) == bad
     assert L.moe_dispatch_backward(4, 64, 2, FAKE, FAKE, FAKE, 3, None, None) == bad
+
+
+def test_coalesced_calls_reject_bad_arguments(m):
+    L = m._lib
+    bad = m.MOE_ERR_INVALID_ARG
+    ws = 1 << 20
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None, None)
+    assert L.moe_layout_coalesced(4, 2, 6, 4, *args) == bad                 # E % R
+    assert L.moe_layout_coalesced(4, 2, 2048, 2, *args) == m.MOE_ERR_UNSUPPORTED
+    assert L.moe_layout_coalesced(4, 2, 8, 2, FAKE, None, *args[2:]) == bad  # null slot_of
+    assert L.moe_layout_coalesced(4, 2, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, FAKE,
+                                  FAKE, ws, None, None) == bad              # crow alignment
+    # the workspace is sized by the rank count: 128 tiles x R int32 at most
+    need = m.moe_layout_workspace_bytes(1 << 20, 8, 32)
+    assert L.moe_layout_coalesced(1 << 20, 8, 256, 32, *args[:8], need - 4, None,
+                                  None) == bad
+    assert L.moe_dispatch_coalesced(4, 12, 2, FAKE, FAKE, 8, FAKE, None, None) == bad  # H % 8
+    assert L.moe_dispatch_coalesced(4, 64, 2, FAKE, FAKE, -1, FAKE, None, None) == bad
+    assert L.moe_dispatch_coalesced(4, 64, 2, FAKE, FAKE, 8, FAKE + 8, None, None) == bad
+    assert L.moe_dispatch_coalesced(4, 64, 40, FAKE, FAKE, 8, FAKE, None,
+                                    None) == m.MOE_ERR_UNSUPPORTED
