@@ -57,10 +57,13 @@ def _bind(path: str) -> ctypes.CDLL:
     L.oracle_dispatch_backward.argtypes = [I, I, I, P, P, P, I]
     L.oracle_layout_coalesced.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
     L.oracle_dispatch_coalesced.argtypes = [I, I, I, P, P, P]
+    L.oracle_combine_coalesced_pre.argtypes = [I, I, I, P, P, P, P, I, P]
+    L.oracle_combine_coalesced_post.argtypes = [I, I, I, P, P, I, P, I]
     for f in ("oracle_layout", "oracle_dispatch", "oracle_dispatch_quant",
               "oracle_combine", "oracle_combine_f64", "oracle_abi_version",
               "oracle_combine_backward", "oracle_dispatch_backward",
-              "oracle_layout_coalesced", "oracle_dispatch_coalesced"):
+              "oracle_layout_coalesced", "oracle_dispatch_coalesced",
+              "oracle_combine_coalesced_pre", "oracle_combine_coalesced_post"):
         getattr(L, f).restype = ctypes.c_int
     return L
 
@@ -227,6 +230,33 @@ def dispatch_coalesced(x_bf16: np.ndarray, crow: np.ndarray, n_rows: int) -> np.
     out = np.zeros((max(T * k, 1), H), np.uint16)
     _check(lib().oracle_dispatch_coalesced(T, H, k, _p(x), _p(cr), _p(out)))
     return out[:n_rows]
+
+
+def combine_coalesced_pre(y_bf16: np.ndarray, slot_of: np.ndarray, topk_w: np.ndarray,
+                          crow: np.ndarray, n_rows: int) -> np.ndarray:
+    """partial[c] = bf16(sum over the slots of row c of w * y), uint16 [n_rows, H]."""
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    cr = np.ascontiguousarray(crow, dtype=np.int32)
+    T, k = so.shape
+    H = y.shape[1]
+    part = np.zeros((max(n_rows, 1), H), np.uint16)
+    _check(lib().oracle_combine_coalesced_pre(T, H, k, _p(y), _p(so), _p(w), _p(cr), n_rows,
+                                              _p(part)))
+    return part[:n_rows]
+
+
+def combine_coalesced_post(partial: np.ndarray, crow: np.ndarray, out_dtype: str = "bf16"):
+    """out[t] = sum over the token's distinct coalesced rows of partial (fp32)."""
+    p = np.ascontiguousarray(partial, dtype=np.uint16)
+    cr = np.ascontiguousarray(crow, dtype=np.int32)
+    T, k = cr.shape
+    H = p.shape[1]
+    out = np.empty((T, H), np.uint16 if out_dtype == "bf16" else np.float32)
+    _check(lib().oracle_combine_coalesced_post(T, H, k, _p(p), _p(cr), p.shape[0], _p(out),
+                                               0 if out_dtype == "bf16" else 1))
+    return out
 
 
 def e4m3_encode(f: np.ndarray) -> np.ndarray:

@@ -28,6 +28,10 @@
  *                          = sum of distinct ranks per token, token order per rank,
  *                          expand consistent with the plain slot map)
  *   oracle_dispatch_coalesced rows equal the owning token's row
+ *   oracle_combine_coalesced_pre/post  one rank (R = 1) reduces to the plain
+ *                          combine; one slot per rank to bf16(w*y) summed in
+ *                          fp32; integer payloads give the exact sum; within
+ *                          a derived bound of the binary64 sum
  */
 #include <float.h>
 #include <math.h>
@@ -483,6 +487,84 @@ int oracle_dispatch_coalesced(int T, int H, int k, const uint16_t *x, const int3
             if (c < 0 || c >= N)
                 return ORACLE_ERR_BAD_INDEX;
             memcpy(recv_c + (int64_t)c * H, x + (int64_t)t * H, sizeof(uint16_t) * (size_t)H);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Rank-coalesced combine: the return path of the coalesced dispatch.  One    */
+/* row per (token, destination rank) comes back, so each rank first reduces  */
+/* the token's slots it holds into that row (RailWave section 3.1, token      */
+/* coalescing; section 3: combine reuses the dispatch metadata).  Reading:    */
+/* the returned row is bf16, like the dispatched payload.                     */
+/*   pre:  partial[c] = bf16( fmaf-sum over j with crow[t,j] == c, in         */
+/*         increasing j, of w[t,j] * y[slot_of[t,j]] ), from +0               */
+/*   post: out[t] = sum over the token's distinct rows c, in order of their   */
+/*         first slot, of float(partial[c]); fp32 adds from +0, one rounding  */
+/*         to the output type                                                 */
+/* ------------------------------------------------------------------------- */
+int oracle_combine_coalesced_pre(int T, int H, int k, const uint16_t *y, const int32_t *slot_of,
+                                 const float *topk_w, const int32_t *crow, int n_rows,
+                                 uint16_t *partial)
+{
+    if (T < 0 || H < 1 || k < 1 || n_rows < 0)
+        return ORACLE_ERR_INVALID_ARG;
+    const int64_t N = (int64_t)T * k;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            const int64_t i = (int64_t)t * k + j;
+            const int32_t c = crow[i];
+            if (c < 0 || c >= n_rows)
+                return ORACLE_ERR_BAD_INDEX;
+            int first = 1;
+            for (int jj = 0; jj < j; ++jj)
+                if (crow[(int64_t)t * k + jj] == c)
+                    first = 0;
+            if (!first)
+                continue;
+            for (int h = 0; h < H; ++h) {
+                float acc = 0.0f;
+                for (int jj = j; jj < k; ++jj) {
+                    const int64_t ii = (int64_t)t * k + jj;
+                    if (crow[ii] != c)
+                        continue;
+                    if (slot_of[ii] < 0 || slot_of[ii] >= N)
+                        return ORACLE_ERR_BAD_INDEX;
+                    acc = fmaf(topk_w[ii], bf16_to_f32(y[(int64_t)slot_of[ii] * H + h]), acc);
+                }
+                partial[(int64_t)c * H + h] = oracle_f32_to_bf16(acc);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_combine_coalesced_post(int T, int H, int k, const uint16_t *partial,
+                                  const int32_t *crow, int n_rows, void *out, int out_dtype)
+{
+    if (T < 0 || H < 1 || k < 1 || n_rows < 0 || (out_dtype != 0 && out_dtype != 1))
+        return ORACLE_ERR_INVALID_ARG;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            const int32_t c = crow[(int64_t)t * k + j];
+            if (c < 0 || c >= n_rows)
+                return ORACLE_ERR_BAD_INDEX;
+        }
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                const int32_t c = crow[(int64_t)t * k + j];
+                int first = 1;
+                for (int jj = 0; jj < j; ++jj)
+                    if (crow[(int64_t)t * k + jj] == c)
+                        first = 0;
+                if (first)
+                    acc = acc + bf16_to_f32(partial[(int64_t)c * H + h]);
+            }
+            if (out_dtype == 0)
+                ((uint16_t *)out)[(int64_t)t * H + h] = oracle_f32_to_bf16(acc);
+            else
+                ((float *)out)[(int64_t)t * H + h] = acc;
         }
     }
     return ORACLE_OK;

@@ -44,6 +44,11 @@ MUTANTS = {
     # coalesced: tokens coalesced per expert instead of per rank
     "coalesced_key": ("            for (int jj = j - 1; jj >= 0; --jj)\n                if (topk_idx[(int64_t)t * k + jj] / El == r)\n                    owner_j = jj;",
                       "            for (int jj = j - 1; jj >= 0; --jj)\n                if (topk_idx[(int64_t)t * k + jj] == topk_idx[i])\n                    owner_j = jj;"),
+    # coalesced combine: each rank returns only its first slot's contribution
+    "pre_first_only": ("for (int jj = j; jj < k; ++jj) {", "for (int jj = j; jj < j + 1; ++jj) {"),
+    # coalesced combine: the token adds its row once per slot, not once per row
+    "post_duplicates": ("if (first)\n                    acc = acc + bf16_to_f32(partial",
+                        "if (1)\n                    acc = acc + bf16_to_f32(partial"),
     # bf16: ties rounded up instead of to even
     "bf16_ties": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (lower >= 0x8000u)"),
 }
@@ -67,7 +72,9 @@ def _pins():
              lambda: tbw.test_combine_backward_matches_autograd(tbw.CASES[1]),
              lambda: tbw.test_dispatch_backward_is_unit_weight_combine(tbw.CASES[1]),
              tco.test_coalesced_hand_worked,
-             lambda: tco.test_coalesced_layout_matches_brute_force(*tco.CASES[7])]
+             lambda: tco.test_coalesced_layout_matches_brute_force(*tco.CASES[7]),
+             lambda: tco.test_coalesced_combine_integer_payload_is_exact(1, 64, 8, 32, 4),
+             lambda: tco.test_coalesced_combine_on_one_rank_is_plain_combine(40, 8, 16)]
     return pins
 
 
