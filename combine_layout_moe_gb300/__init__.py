@@ -42,6 +42,8 @@ SIGNATURES = {
     "moe_layout_coalesced": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P],
                              ctypes.c_int),
     "moe_dispatch_coalesced": ([_I, _I, _I, _P, _P, _I, _P, _U32P, _P], ctypes.c_int),
+    "moe_combine_coalesced": ([_I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _I, _U32P, _P],
+                              ctypes.c_int),
     "moe_dispatch_combine_flagged": ([_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_uint32,
                                       ctypes.c_uint64, ctypes.c_int64, _U32P, _P], ctypes.c_int),
 }
@@ -225,6 +227,32 @@ def moe_dispatch_coalesced(x: torch.Tensor, crow: torch.Tensor, rows: int, *,
     return recv_c
 
 
+def moe_combine_coalesced(y: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.Tensor,
+                          co: CoalescedLayout, rows: int, *,
+                          partial: Optional[torch.Tensor] = None,
+                          out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                          err_word: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None):
+    """Per-rank pre-reduction into `partial` (bf16 [rows, H]), then the sum of
+    each token's distinct coalesced rows.  Returns (out, partial)."""
+    T, k = slot_of.shape
+    H = y.shape[1]
+    _want(y, "y", torch.bfloat16)
+    _want(slot_of, "slot_of", torch.int32, (T, k))
+    _want(topk_w, "topk_w", torch.float32, (T, k))
+    if partial is None:
+        partial = torch.empty((rows, H), dtype=torch.bfloat16, device=y.device)
+    elif partial.shape[0] < rows:
+        raise ValueError("partial has fewer than `rows` rows")
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=y.device)
+    code = MOE_OUT_F32 if out.dtype == torch.float32 else MOE_OUT_BF16
+    _check(_lib.moe_combine_coalesced(T, H, k, _ptr(y), _ptr(slot_of), _ptr(topk_w),
+                                      _ptr(co.crow), rows, _ptr(partial), _ptr(out), code,
+                                      _ptr(err_word), _stream(stream)), "moe_combine_coalesced")
+    return out, partial
+
+
 def moe_dispatch(x: torch.Tensor, slot_of: torch.Tensor, *, recv: Optional[torch.Tensor] = None,
                  err_word: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
@@ -393,6 +421,6 @@ __all__ = [
     "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
     "moe_combine", "moe_read_error", "moe_flag_words", "FlagWords",
     "moe_combine_backward", "moe_dispatch_backward",
-    "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced",
+    "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_combine_coalesced",
     "moe_dispatch_combine_flagged", "LIB_PATH", "SIGNATURES",
 ]

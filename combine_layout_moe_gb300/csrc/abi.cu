@@ -162,6 +162,27 @@ moe_status moe_dispatch_coalesced(int T, int H, int k, const void *x, const int3
                                                     stream));
 }
 
+moe_status moe_combine_coalesced(int T, int H, int k, const void *y, const int32_t *slot_of,
+                                 const float *topk_w, const int32_t *crow, int rows,
+                                 void *partial, void *out, int out_dtype, uint32_t *err_word,
+                                 cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0 || rows < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (out_dtype != MOE_OUT_BF16 && out_dtype != MOE_OUT_F32)
+        return MOE_ERR_INVALID_ARG;
+    if (k > 32)
+        return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!y || !slot_of || !topk_w || !crow || !partial || !out))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(partial, 16) || !aligned(out, 16) || !aligned(slot_of, 4) ||
+        !aligned(topk_w, 4) || !aligned(crow, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine_coalesced(T, H, k, y, slot_of, topk_w, crow, rows,
+                                                   partial, out, out_dtype == MOE_OUT_F32,
+                                                   err_word, stream));
+}
+
 moe_status moe_dispatch_quant(int T, int H, int k, const void *x, const int32_t *slot_of,
                               uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
                               cudaStream_t stream)

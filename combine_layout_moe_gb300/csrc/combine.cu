@@ -135,7 +135,10 @@ constexpr int CT_CONSUMERS = MOE_CT_CONSUMERS;
 constexpr int CT_THREADS = 32 * (CT_CONSUMERS + 1);
 constexpr int CT_STAGES = MOE_CT_STAGES;
 constexpr int CT_STAGE_TARGET = MOE_CT_STAGE_TARGET;  // bytes of k row chunks per stage
-constexpr int CT_HDR_WORDS = 36;  // per stage: 32 weights, valid-slot mask, padding
+// Stage header words: [0, 32) slot weights, 32 valid-slot mask, 33 group-leader
+// mask, [36, 68) member mask of each leader's group, [68, 100) its output row.
+constexpr int CT_HDR_WORDS = 100;
+constexpr int CT_HDR_OK = 32, CT_HDR_LEAD = 33, CT_HDR_MEMB = 36, CT_HDR_ROW = 68;
 constexpr int CT_BAR_BYTES = 16 * CT_STAGES;
 constexpr int CT_HDR_BYTES = 4 * CT_HDR_WORDS * CT_STAGES;
 constexpr int CT_PREFIX = (CT_BAR_BYTES + CT_HDR_BYTES + 127) / 128 * 128;
@@ -176,12 +179,22 @@ __device__ __forceinline__ void advance(int64_t &t, int &c, int step, int nchunk
     } while (0)
 #endif
 
-template <int KMAX>
+// What a unit (token t, chunk c) of the bulk combine reduces.
+//   CB_PLAIN  out[t] from slots slot_of[t, :], weights topk_w[t, :] (null: 1)
+//   CB_PRE    the rank-side pre-reduction of the coalesced combine: the token's
+//             slots are grouped by coalesced row crow[t, :]; each group's
+//             weighted sum goes to out[crow] (bf16), groups led by their first
+//             slot, members folded in increasing j
+//   CB_POST   out[t] from the token's distinct coalesced rows crow[t, :] (each
+//             once, at its first slot), unit weights
+enum { CB_PLAIN = 0, CB_PRE = 1, CB_POST = 2 };
+
+template <int KMAX, int MODE>
 __global__ void __launch_bounds__(CT_THREADS, 1)
     combine_bulk_kernel(const uint8_t *__restrict__ y, const int32_t *__restrict__ slot_of,
-                        const float *__restrict__ topk_w, void *__restrict__ out, int out_f32,
-                        int T, int H, int k, int CH, int nchunks, int64_t units,
-                        uint32_t *err_word)
+                        const float *__restrict__ topk_w, const int32_t *__restrict__ crow,
+                        void *__restrict__ out, int out_f32, int T, int H, int k, int bound,
+                        int gbound, int CH, int nchunks, int64_t units, uint32_t *err_word)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t bars = smem_addr(smem);
@@ -192,7 +205,6 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
     const uint32_t stage_bytes = (uint32_t)k * CH;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t rowbytes = 2 * (int64_t)H;
-    const int N = T * k;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < CT_STAGES; ++s) {
@@ -219,15 +231,31 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         int64_t t = u0 / nchunks;
         int c = (int)(u0 - t * nchunks);
         const bool kl = lane < k;
-        // a null weight array means unit weights (the gradient of dispatch)
-        auto weight = [&](int64_t tok) {
-            return topk_w ? ld_nc_f32(topk_w + tok * k + lane) : 1.0f;
+        const unsigned kmask = k >= 32 ? FULL_MASK : (1u << k) - 1u;
+        // this lane's slot of token `row`: source row, weight, whether it takes
+        // part, and (CB_PRE) its group's output row (called by the whole warp)
+        auto row_info = [&](int64_t row, int32_t &slot, float &w, bool &want, int32_t &grp) {
+            grp = 0;
+            if (MODE == CB_POST) {
+                slot = kl ? ld_nc_s32(crow + row * k + lane) : 0;
+                w = 1.0f;
+                const unsigned same = __match_any_sync(FULL_MASK, slot) & kmask;
+                want = kl && (same & lanemask_lt()) == 0;
+            } else {
+                slot = kl ? ld_nc_s32(slot_of + row * k + lane) : 0;
+                // a null weight array means unit weights (the gradient of dispatch)
+                w = kl ? (topk_w ? ld_nc_f32(topk_w + row * k + lane) : 1.0f) : 0.0f;
+                want = kl;
+                if (MODE == CB_PRE)
+                    grp = kl ? ld_nc_s32(crow + row * k + lane) : 0;
+            }
         };
-        int32_t cur_slot = kl ? ld_nc_s32(slot_of + t * k + lane) : 0;
-        float cur_w = kl ? weight(t) : 0.0f;
-        const bool has_next = t + 1 < T;
-        int32_t nxt_slot = kl && has_next ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
-        float nxt_w = kl && has_next ? weight(t + 1) : 0.0f;
+        int32_t cur_slot, nxt_slot = 0, cur_grp, nxt_grp = 0;
+        float cur_w, nxt_w = 0.0f;
+        bool cur_want, nxt_want = false;
+        row_info(t, cur_slot, cur_w, cur_want, cur_grp);
+        if (t + 1 < T)
+            row_info(t + 1, nxt_slot, nxt_w, nxt_want, nxt_grp);
         int64_t n = 0;
         bool timed_out = false;
         for (; n < nloc; ++n) {
@@ -237,9 +265,10 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                 if (t != t_prev) {
                     cur_slot = nxt_slot;
                     cur_w = nxt_w;
-                    const bool more = kl && t + 1 < T;
-                    nxt_slot = more ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
-                    nxt_w = more ? weight(t + 1) : 0.0f;
+                    cur_want = nxt_want;
+                    cur_grp = nxt_grp;
+                    if (t + 1 < T)
+                        row_info(t + 1, nxt_slot, nxt_w, nxt_want, nxt_grp);
                 }
             }
             const int s = (int)(n % CT_STAGES);
@@ -249,9 +278,23 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                 break;
             }
             const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
-            const bool ok = kl && (unsigned)cur_slot < (unsigned)N;
+            const bool ok = cur_want && (unsigned)cur_slot < (unsigned)bound &&
+                            (MODE != CB_PRE || (unsigned)cur_grp < (unsigned)gbound);
             const unsigned okmask = __ballot_sync(FULL_MASK, ok);
+            const unsigned wantmask = __ballot_sync(FULL_MASK, cur_want);
             float *h = hdr + s * CT_HDR_WORDS;
+            if (MODE == CB_PRE) {
+                // groups of valid slots sharing a coalesced row, led by their first slot
+                const unsigned same = __match_any_sync(FULL_MASK, ok ? cur_grp : -1) & okmask;
+                const bool lead = ok && (same & lanemask_lt()) == 0;
+                uint32_t *hu = reinterpret_cast<uint32_t *>(h);
+                hu[CT_HDR_MEMB + lane] = lead ? same : 0u;
+                hu[CT_HDR_ROW + lane] = (uint32_t)cur_grp;
+                const unsigned leaders = __ballot_sync(FULL_MASK, lead);
+                if (lane == 0)
+                    hu[CT_HDR_LEAD] = leaders;
+                __syncwarp();
+            }
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) {
                 const float wj = __shfl_sync(FULL_MASK, cur_w, j);
@@ -259,8 +302,8 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                     h[j] = wj;
             }
             if (lane == 0) {
-                reinterpret_cast<uint32_t *>(h)[32] = okmask;
-                if (c == 0 && okmask != (k >= 32 ? FULL_MASK : ((1u << k) - 1u)))
+                reinterpret_cast<uint32_t *>(h)[CT_HDR_OK] = okmask;
+                if (c == 0 && okmask != wantmask)
                     report(err_word, MOE_ERRBIT_BAD_INDEX);
                 mbar_arrive_expect_tx(full(s), (uint32_t)__popc(okmask) * cb);
             }
@@ -297,7 +340,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         if (n == 0 && lane == 0)
             CT_TRACE(1);
         const float *h = hdr + s * CT_HDR_WORDS;
-        const unsigned okmask = reinterpret_cast<const uint32_t *>(h)[32];
+        const unsigned okmask = reinterpret_cast<const uint32_t *>(h)[CT_HDR_OK];
         float w[KMAX];
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
@@ -305,38 +348,73 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         const int cb = (int)min((int64_t)CH, rowbytes - (int64_t)c * CH);
         const uint32_t base = stages + (uint32_t)s * stage_bytes;
         const int64_t out_elem0 = t * H + (int64_t)c * (CH / 2);
-        for (int v = lane; v < cb / 16; v += 32) {
-            float acc[8];
+        if (MODE == CB_PRE) {
+            // one output row per group; members in increasing slot order
+            const uint32_t *hu = reinterpret_cast<const uint32_t *>(h);
+            const unsigned leaders = hu[CT_HDR_LEAD];
+            const int64_t col0 = (int64_t)c * (CH / 2);
+            for (int v = lane; v < cb / 16; v += 32) {
+                for (unsigned ls = leaders; ls; ls &= ls - 1) {
+                    const int o = __ffs(ls) - 1;
+                    float acc[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                acc[i] = 0.0f;
+                    for (int i = 0; i < 8; ++i)
+                        acc[i] = 0.0f;
+                    for (unsigned mm = hu[CT_HDR_MEMB + o]; mm; mm &= mm - 1) {
+                        const int j = __ffs(mm) - 1;
+                        const float wj = h[j];
+                        const uint4 q = lds128(base + (uint32_t)j * CH + (uint32_t)v * 16);
+                        const uint32_t p[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                if (j < k && ((okmask >> j) & 1u)) {
-                    const uint4 q = lds128(base + (uint32_t)j * CH + (uint32_t)v * 16);
-                    const uint32_t p[4] = {q.x, q.y, q.z, q.w};
+                        for (int hh = 0; hh < 4; ++hh) {
+                            acc[2 * hh] = __fmaf_rn(wj, bf16lo(p[hh]), acc[2 * hh]);
+                            acc[2 * hh + 1] = __fmaf_rn(wj, bf16hi(p[hh]), acc[2 * hh + 1]);
+                        }
+                    }
+                    uint32_t rr[4];
 #pragma unroll
                     for (int hh = 0; hh < 4; ++hh) {
-                        acc[2 * hh] = __fmaf_rn(w[j], bf16lo(p[hh]), acc[2 * hh]);
-                        acc[2 * hh + 1] = __fmaf_rn(w[j], bf16hi(p[hh]), acc[2 * hh + 1]);
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * hh], acc[2 * hh + 1]);
+                        rr[hh] = *reinterpret_cast<const uint32_t *>(&b);
                     }
+                    const int64_t e0 = (int64_t)(int32_t)hu[CT_HDR_ROW + o] * H + col0 + (int64_t)v * 8;
+                    st_v4(static_cast<__nv_bfloat16 *>(out) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
                 }
             }
-            const int64_t e0 = out_elem0 + (int64_t)v * 8;
-            if (out_f32) {
-                float *o = static_cast<float *>(out) + e0;
-                st_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                                    __float_as_uint(acc[2]), __float_as_uint(acc[3])));
-                st_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
-                                        __float_as_uint(acc[6]), __float_as_uint(acc[7])));
-            } else {
-                uint32_t rr[4];
+        } else {
+            for (int v = lane; v < cb / 16; v += 32) {
+                float acc[8];
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * hh], acc[2 * hh + 1]);
-                    rr[hh] = *reinterpret_cast<const uint32_t *>(&b);
+                for (int i = 0; i < 8; ++i)
+                    acc[i] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < k && ((okmask >> j) & 1u)) {
+                        const uint4 q = lds128(base + (uint32_t)j * CH + (uint32_t)v * 16);
+                        const uint32_t p[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int hh = 0; hh < 4; ++hh) {
+                            acc[2 * hh] = __fmaf_rn(w[j], bf16lo(p[hh]), acc[2 * hh]);
+                            acc[2 * hh + 1] = __fmaf_rn(w[j], bf16hi(p[hh]), acc[2 * hh + 1]);
+                        }
+                    }
                 }
-                st_v4(static_cast<__nv_bfloat16 *>(out) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
+                const int64_t e0 = out_elem0 + (int64_t)v * 8;
+                if (out_f32) {
+                    float *o = static_cast<float *>(out) + e0;
+                    st_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                                        __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+                    st_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                                            __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+                } else {
+                    uint32_t rr[4];
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * hh], acc[2 * hh + 1]);
+                        rr[hh] = *reinterpret_cast<const uint32_t *>(&b);
+                    }
+                    st_v4(static_cast<__nv_bfloat16 *>(out) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
+                }
             }
         }
         __syncwarp();
@@ -350,10 +428,13 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
 #endif
 }
 
-template <int KMAX>
-static cudaError_t launch_combine_bulk(int T, int H, int k, const void *y, const int32_t *slot_of,
-                                       const float *topk_w, void *out, bool out_f32,
-                                       uint32_t *err_word, cudaStream_t stream)
+// T tokens; slot indices must lie in [0, bound) and (CB_PRE) output rows in
+// [0, gbound).
+template <int KMAX, int MODE>
+static cudaError_t launch_combine_bulk(int T, int H, int k, const void *y,
+                                       const int32_t *slot_of, const float *topk_w,
+                                       const int32_t *crow, void *out, bool out_f32, int bound,
+                                       int gbound, uint32_t *err_word, cudaStream_t stream)
 {
     // Equal chunks (multiples of 16 bytes) of about CT_STAGE_TARGET / k bytes:
     // the fewest chunks per row whose k-row stage fits the target.
@@ -368,20 +449,21 @@ static cudaError_t launch_combine_bulk(int T, int H, int k, const void *y, const
     nchunks = (rowbytes + CH - 1) / CH;
     const int64_t units = (int64_t)T * nchunks;
     const size_t smem = CT_PREFIX + (size_t)CT_STAGES * k * CH;
-    cudaError_t e = cudaFuncSetAttribute(combine_bulk_kernel<KMAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = combine_bulk_kernel<KMAX, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess)
         return e;
     int per_sm = 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_bulk_kernel<KMAX>, CT_THREADS,
-                                                      smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CT_THREADS, smem) !=
+            cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const int64_t g = units < cap ? units : cap;
-    return launch_pdl(combine_bulk_kernel<KMAX>, dim3((unsigned)g), dim3(CT_THREADS), smem, stream,
-                      static_cast<const uint8_t *>(y), slot_of, topk_w, out, out_f32 ? 1 : 0, T, H,
-                      k, CH, nchunks, units, err_word);
+    return launch_pdl(kern, dim3((unsigned)g), dim3(CT_THREADS), smem, stream,
+                      static_cast<const uint8_t *>(y), slot_of, topk_w, crow, out,
+                      out_f32 ? 1 : 0, T, H, k, bound, gbound, CH, nchunks, units, err_word);
 }
 
 template <int KC, int U>
@@ -674,16 +756,46 @@ cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *sl
 {
     if (T == 0)
         return cudaSuccess;
+    const int N = T * k;
     if (k <= 8)
-        return launch_combine_bulk<8>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);
+        return launch_combine_bulk<8, CB_PLAIN>(T, H, k, y, slot_of, topk_w, nullptr, out,
+                                                out_f32, N, 0, err_word, stream);
     if (k <= 32)
-        return launch_combine_bulk<32>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);
+        return launch_combine_bulk<32, CB_PLAIN>(T, H, k, y, slot_of, topk_w, nullptr, out,
+                                                 out_f32, N, 0, err_word, stream);
     // KC x U ~ 16 independent 16-byte loads in flight per lane.
-    if (k <= 2)
-        return launch_combine_t<2, 4>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);
-    if (k <= 4)
-        return launch_combine_t<4, 4>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);
     return launch_combine_t<8, 2>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);
+}
+
+// Coalesced combine: the rank-side pre-reduction into `partial` (one bf16 row
+// per coalesced row), then the token-side sum of each token's distinct rows.
+template <int KMAX>
+static cudaError_t launch_combine_coalesced_t(int T, int H, int k, const void *y,
+                                              const int32_t *slot_of, const float *topk_w,
+                                              const int32_t *crow, int rows, void *partial,
+                                              void *out, bool out_f32, uint32_t *err_word,
+                                              cudaStream_t stream)
+{
+    cudaError_t e = launch_combine_bulk<KMAX, CB_PRE>(T, H, k, y, slot_of, topk_w, crow, partial,
+                                                      false, T * k, rows, err_word, stream);
+    if (e != cudaSuccess)
+        return e;
+    return launch_combine_bulk<KMAX, CB_POST>(T, H, k, partial, nullptr, nullptr, crow, out,
+                                              out_f32, rows, 0, err_word, stream);
+}
+
+cudaError_t launch_combine_coalesced(int T, int H, int k, const void *y, const int32_t *slot_of,
+                                     const float *topk_w, const int32_t *crow, int rows,
+                                     void *partial, void *out, bool out_f32, uint32_t *err_word,
+                                     cudaStream_t stream)
+{
+    if (T == 0)
+        return cudaSuccess;
+    if (k <= 8)
+        return launch_combine_coalesced_t<8>(T, H, k, y, slot_of, topk_w, crow, rows, partial,
+                                             out, out_f32, err_word, stream);
+    return launch_combine_coalesced_t<32>(T, H, k, y, slot_of, topk_w, crow, rows, partial, out,
+                                          out_f32, err_word, stream);
 }
 
 }  // namespace moe

@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(DC_THREADS)
     }
 }
 
-int flagged_chunks(int H) { return (H / 8 + 32 * DC_U - 1) / (32 * DC_U); }
+int flagged_chunks(int H) { return (2 * H + DC_CHUNK - 1) / DC_CHUNK; }
 
 cudaError_t launch_dispatch_combine_flagged(int T, int H, int k, const void *x,
                                             const int32_t *slot_of, const float *topk_w,

@@ -36,6 +36,11 @@ cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *sl
                            const float *topk_w, void *out, bool out_f32,
                            uint32_t *err_word, cudaStream_t stream);
 
+cudaError_t launch_combine_coalesced(int T, int H, int k, const void *y, const int32_t *slot_of,
+                                     const float *topk_w, const int32_t *crow, int rows,
+                                     void *partial, void *out, bool out_f32, uint32_t *err_word,
+                                     cudaStream_t stream);
+
 cudaError_t launch_combine_backward(int T, int H, int k, const void *dout, const void *y,
                                     const int32_t *slot_of, const float *topk_w, void *dy,
                                     float *dw, uint32_t *err_word, cudaStream_t stream);

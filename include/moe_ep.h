@@ -257,6 +257,37 @@ MOE_API moe_status moe_dispatch_coalesced(int T, int H, int k, const void *x,
                                   uint32_t *err_word, cudaStream_t stream);
 
 /*
+ * moe_combine_coalesced -- the return path of the coalesced dispatch: each
+ * destination rank pre-reduces a token's slots it holds into the token's
+ * coalesced row, then the token sums its rows.
+ *
+ * RailWave, section 3.1 (token coalescing) and section 3 (combine reuses the
+ * dispatch metadata).  Reading: the returned row is bf16, like the payload.
+ *
+ *   y        [T*k, H]  bf16 expert outputs in plain receive order
+ *   slot_of  [T, k]    from moe_layout
+ *   topk_w   [T, k]    fp32 router weights
+ *   crow     [T, k]    from moe_layout_coalesced
+ *   rows     capacity of partial in rows (crow < rows; T * min(k, R) always
+ *            suffices)
+ *   partial  [rows, H] out: bf16; partial[c] = bf16(sum over the slots j of
+ *            row c's token with crow[t, j] == c, in increasing j, of
+ *            w[t, j] * y[slot_of[t, j]]), fp32 fused multiply-adds from +0
+ *   out      [T, H]    out: bf16 (MOE_OUT_BF16) or fp32 (MOE_OUT_F32); fp32
+ *            sum from +0 of the token's distinct rows, in order of their
+ *            first slot, rounded once
+ *
+ * Two launches, both token-major.  1 <= k <= 32 (larger k:
+ * MOE_ERR_UNSUPPORTED); H % 8 == 0.  Rows of crow outside [0, rows) set
+ * MOE_ERRBIT_BAD_INDEX and are skipped.  Not bit-identical to moe_combine:
+ * each rank's share is rounded to bf16.
+ */
+MOE_API moe_status moe_combine_coalesced(int T, int H, int k, const void *y,
+                                 const int32_t *slot_of, const float *topk_w,
+                                 const int32_t *crow, int rows, void *partial, void *out,
+                                 int out_dtype, uint32_t *err_word, cudaStream_t stream);
+
+/*
  * moe_dispatch_combine_flagged -- dispatch, an identity expert and combine in
  * one persistent kernel, with Data-as-Flag readiness instead of a barrier.
  *

@@ -130,3 +130,11 @@ def test_coalesced_calls_reject_bad_arguments(m):
     assert L.moe_dispatch_coalesced(4, 64, 2, FAKE, FAKE, 8, FAKE + 8, None, None) == bad
     assert L.moe_dispatch_coalesced(4, 64, 40, FAKE, FAKE, 8, FAKE, None,
                                     None) == m.MOE_ERR_UNSUPPORTED
+    # coalesced combine: bad dtype, k above 32, misaligned partial
+    cargs = (FAKE, FAKE, FAKE, FAKE, 8)
+    assert L.moe_combine_coalesced(4, 64, 2, *cargs, FAKE, FAKE, 2, None, None) == bad
+    assert L.moe_combine_coalesced(4, 64, 40, *cargs, FAKE, FAKE, 0, None,
+                                   None) == m.MOE_ERR_UNSUPPORTED
+    assert L.moe_combine_coalesced(4, 64, 2, *cargs, FAKE + 8, FAKE, 0, None, None) == bad
+    assert L.moe_combine_coalesced(4, 64, 2, FAKE, FAKE, FAKE, FAKE, -1, FAKE, FAKE, 0, None,
+                                   None) == bad

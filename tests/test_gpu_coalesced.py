@@ -193,3 +193,83 @@ def test_coalesced_dispatch_rejects_large_k():
     with pytest.raises(m.MoeError) as ei:
         m.moe_dispatch_coalesced(x, crow, 2)
     assert ei.value.status == m.MOE_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ combine
+
+def _coalesced_combine_case(w, y, out_dtype):
+    m = cl()
+    lay, co, nc = assert_coalesced_equal(w.topk_idx, w.E, w.R)
+    rows = w.T * min(w.k, w.R)
+    wt = torch.from_numpy(np.ascontiguousarray(w.topk_w)).cuda()
+    out, part = m.moe_combine_coalesced(bf16_dev(y), lay.slot_of, wt, co, rows,
+                                        out_dtype=out_dtype)
+    slot_of, crow = lay.slot_of.cpu().numpy(), co.crow.cpu().numpy()
+    ref_part = oracle.combine_coalesced_pre(y, slot_of, w.topk_w, crow, nc)
+    assert np.array_equal(bits(part)[:nc], ref_part)
+    ref = oracle.combine_coalesced_post(ref_part, crow,
+                                        "bf16" if out_dtype == torch.bfloat16 else "f32")
+    got = bits(out) if out_dtype == torch.bfloat16 else out.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32 if got.dtype == np.float32 else np.uint16),
+                          ref.view(np.uint32 if ref.dtype == np.float32 else np.uint16))
+    return lay, co, out
+
+
+@pytest.mark.parametrize("name", CONFIG_ORDER)
+def test_coalesced_combine_matches_oracle(name):
+    from workloads.gen import expert_output
+    w = workload(name)
+    _coalesced_combine_case(w, expert_output(w.N, w.H, seed=w.seed + 7), torch.bfloat16)
+
+
+@pytest.mark.parametrize("name", ["tiny", "glm45_air"])
+def test_coalesced_combine_f32_matches_oracle(name):
+    from workloads.gen import expert_output
+    w = workload(name)
+    _coalesced_combine_case(w, expert_output(w.N, w.H, seed=w.seed + 9), torch.float32)
+
+
+COMBINE_FUZZ = [  # (seed, T, H, k, E, R)
+    (31, 1, 8, 1, 1, 1), (32, 17, 24, 3, 12, 4), (33, 300, 1000, 8, 64, 8),
+    (34, 2000, 2048, 2, 8, 8), (35, 700, 7176, 8, 256, 32), (36, 64, 4096, 32, 64, 16),
+    (37, 5, 16384, 6, 6, 3), (38, 900, 512, 16, 32, 1), (39, 3000, 128, 12, 48, 48),
+]
+
+
+@pytest.mark.parametrize("case", COMBINE_FUZZ, ids=[f"s{c[0]}_T{c[1]}_H{c[2]}_k{c[3]}_R{c[5]}" for c in COMBINE_FUZZ])
+def test_coalesced_combine_fuzz(case):
+    from workloads.gen import expert_output
+    seed, T, H, k, E, R = case
+    w = random_case(seed, T, H, k, E, R)
+    _coalesced_combine_case(w, expert_output(T * k, H, seed=seed), torch.bfloat16)
+
+
+def test_coalesced_combine_one_rank_equals_plain_combine():
+    from workloads.gen import expert_output
+    m = cl()
+    w = random_case(41, 1500, 1024, 8, 16, 1)
+    y = expert_output(w.N, w.H, seed=3)
+    lay, co, out = _coalesced_combine_case(w, y, torch.bfloat16)
+    wt = torch.from_numpy(np.ascontiguousarray(w.topk_w)).cuda()
+    plain = m.moe_combine(bf16_dev(y), lay.slot_of, wt)
+    assert torch.equal(out.view(torch.int16), plain.view(torch.int16))
+
+
+def test_coalesced_combine_empty_and_bad_rows():
+    m = cl()
+    d = torch.zeros((0, 2), dtype=torch.int32, device="cuda")
+    co = m.moe_layout_coalesced(d, d, 8, 2)
+    out, _ = m.moe_combine_coalesced(torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda"),
+                                     d, torch.zeros((0, 2), dtype=torch.float32, device="cuda"),
+                                     co, 0)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 64)
+    # a capacity below Nc: the rows past it are neither computed nor read
+    err = m.new_error_word()
+    idx = np.array([[0, 2], [1, 3], [2, 2]], np.int32)   # E=4, R=2: Nc = 5
+    lay = m.moe_layout(i32_dev(idx), 4, 2)
+    co = m.moe_layout_coalesced(i32_dev(idx), lay.slot_of, 4, 2)
+    y = torch.ones((6, 64), dtype=torch.bfloat16, device="cuda")
+    wt = torch.ones((3, 2), dtype=torch.float32, device="cuda")
+    m.moe_combine_coalesced(y, lay.slot_of, wt, co, 3, err_word=err)
+    assert m.moe_read_error(err) == m.MOE_ERRBIT_BAD_INDEX
