@@ -17,6 +17,11 @@ rank runs its own replica).  `e2e` repeats the
 step through the public API with each step's inputs copied from pinned host
 memory and its combined output copied back, pipelined over three streams.
 
+--variant coalesced times the rank-coalesced path instead (bf16 workloads):
+layout -> coalesced layout -> coalesced dispatch (one row per token and
+destination rank), then the coalesced combine (per-rank pre-reduction, then
+the per-token sum).  The default line is the plain path.
+
 --impl reference times the CPU oracle (the plain C statement of the method) on
 the same metric: every step is a bounded sample of the same workload recipe.
 
@@ -55,6 +60,11 @@ def kernel_bytes(name: str, T: int, H: int, k: int, E: int, R: int = 1) -> int:
     dispatch_bf16  reads x and slot_of once, writes k copies of every row
     dispatch_fp8   reads x and slot_of, writes k copies of the codes and scales
     combine        reads k rows per token, slot_of and weights, writes one row
+    The coalesced kernels also depend on Nc, the number of coalesced rows:
+    dispatch_coalesced  reads x and crow, writes Nc rows
+    combine_coalesced   pre-reduction: reads k rows per token, slot_of, weights
+                        and crow, writes Nc rows; then reads the Nc rows and
+                        crow, writes one row per token
     """
     N = T * k
     if name == "layout_count":
@@ -67,6 +77,15 @@ def kernel_bytes(name: str, T: int, H: int, k: int, E: int, R: int = 1) -> int:
         return 2 * T * H + 4 * N + N * H + 4 * N * (H // 128)
     if name == "combine":
         return 2 * N * H + 8 * N + 2 * T * H
+    raise KeyError(name)
+
+
+def coalesced_bytes(name: str, T: int, H: int, k: int, Nc: int) -> int:
+    N = T * k
+    if name == "dispatch_coalesced":
+        return 2 * T * H + 4 * N + 2 * Nc * H
+    if name == "combine_coalesced":
+        return (2 * N * H + 12 * N + 2 * Nc * H) + (2 * Nc * H + 4 * N + 2 * T * H)
     raise KeyError(name)
 
 
@@ -291,7 +310,8 @@ def run_gpu(args):
 
     name = args.config
     c = CONFIGS[name]
-    fp8 = c["payload"] == "fp8"
+    coal = args.variant == "coalesced"
+    fp8 = c["payload"] == "fp8" and not coal   # the coalesced variant moves bf16 rows
     w = make_workload(name, seed=args.seed + rank)
     T, H, k, E, R, N = w.T, w.H, w.k, w.E, w.R, w.N
 
@@ -307,9 +327,19 @@ def run_gpu(args):
                    torch.empty(R + 1, dtype=torch.int32, device=dev),
                    torch.empty((T, k), dtype=torch.int32, device=dev),
                    torch.empty(T * k, dtype=torch.int32, device=dev))
+    rows = T * min(k, R)   # coalesced rows: at most one per token and rank
     if fp8:
         recv_q = torch.empty((N, H), dtype=torch.uint8, device=dev)
         recv_s = torch.empty((N, H // 128), dtype=torch.float32, device=dev)
+    elif coal:
+        recv = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        partial = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        wsc = m.new_workspace(m.moe_layout_workspace_bytes(T, k, R), dev)
+        co = m.CoalescedLayout(torch.empty(R, dtype=torch.int32, device=dev),
+                               torch.empty(R + 1, dtype=torch.int32, device=dev),
+                               torch.empty((T, k), dtype=torch.int32, device=dev),
+                               torch.empty(T * k, dtype=torch.int32, device=dev),
+                               torch.empty(T * k, dtype=torch.int32, device=dev))
     else:
         recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -329,9 +359,21 @@ def run_gpu(args):
     if fp8:
         disp_fn, disp_args = L.moe_dispatch_quant, (T, H, k, P(x), P(lay.slot_of), P(recv_q),
                                                     P(recv_s), P(err), cs)
+    elif coal:
+        disp_fn, disp_args = L.moe_dispatch_coalesced, (T, H, k, P(x), P(co.crow), rows, P(recv),
+                                                        P(err), cs)
     else:
         disp_fn, disp_args = L.moe_dispatch, (T, H, k, P(x), P(lay.slot_of), P(recv), P(err), cs)
-    comb_args = (T, H, k, P(y), P(lay.slot_of), P(wt), P(out), m.MOE_OUT_BF16, P(err), cs)
+    if coal:
+        coal_args = (T, k, E, R, P(idx), P(lay.slot_of), P(co.rank_counts_c),
+                     P(co.rank_offsets_c), P(co.crow), P(co.src_pair_c), P(co.expand), P(wsc),
+                     wsc.numel(), P(err), cs)
+        comb_fn, comb_args = L.moe_combine_coalesced, (T, H, k, P(y), P(lay.slot_of), P(wt),
+                                                       P(co.crow), rows, P(partial), P(out),
+                                                       m.MOE_OUT_BF16, P(err), cs)
+    else:
+        comb_fn, comb_args = L.moe_combine, (T, H, k, P(y), P(lay.slot_of), P(wt), P(out),
+                                             m.MOE_OUT_BF16, P(err), cs)
 
     def call(fn, a):
         st = fn(*a)
@@ -340,12 +382,14 @@ def run_gpu(args):
 
     def layout_only():
         call(L.moe_layout, lay_args)
+        if coal:
+            call(L.moe_layout_coalesced, coal_args)
 
     def dispatch_only():
         call(disp_fn, disp_args)
 
     def combine_only():
-        call(L.moe_combine, comb_args)
+        call(comb_fn, comb_args)
 
     def dirty_flush():
         # write 2xL2: the next kernel starts with L2 full of dirty foreign lines
@@ -396,6 +440,7 @@ def run_gpu(args):
     bits = m.moe_read_error(err)
     if bits:
         raise RuntimeError(f"device error bits {bits:#x} during warm-up")
+    Nc = int(co.rank_offsets_c[R].item()) if coal else N
 
     barrier()
     torch.cuda.synchronize()
@@ -424,19 +469,24 @@ def run_gpu(args):
     t_disp = [e[1].elapsed_time(e[2]) for e in evs]
 
     # roofline of the dominant kernel: combine is timed alone inside the timed
-    # steps; dispatch (when it dominates) in the breakdown pass
-    d_name = "dispatch_fp8" if fp8 else "dispatch_bf16"
+    # steps; dispatch (when it dominates) in the breakdown pass.  In the
+    # coalesced variant the combine segment is its two launches (pre-reduction
+    # and per-token sum), measured together.
+    d_name = "dispatch_fp8" if fp8 else ("dispatch_coalesced" if coal else "dispatch_bf16")
+    c_name = "combine_coalesced" if coal else "combine"
     avg_d, avg_c = statistics.mean(t_disp), statistics.mean(t_comb)
     if avg_c >= avg_d:
-        dom, dom_ms, source = "combine", avg_c, "timed steps"
+        dom, dom_ms, source = c_name, avg_c, "timed steps"
     else:
         dom, dom_ms, source = d_name, avg_d, "breakdown pass (one event pair per kernel)"
-    dom_bytes = kernel_bytes(dom, T, H, k, E, R)
+    dom_bytes = (coalesced_bytes(dom, T, H, k, Nc) if coal else kernel_bytes(dom, T, H, k, E, R))
     peak, peak_kind = measured_peak_gbs()
     achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
     kern_name = {"dispatch_bf16": "dispatch_bulk_kernel", "dispatch_fp8": "dispatch_fp8_kernel",
-                 "combine": "combine_bulk_kernel"}[dom]
-    tr = recorded_traffic(kern_name)
+                 "combine": "combine_bulk_kernel",
+                 "dispatch_coalesced": "dispatch_bulk_kernel<coalesced>",
+                 "combine_coalesced": "combine_bulk_kernel<pre> + combine_bulk_kernel<post>"}[dom]
+    tr = None if coal else recorded_traffic(kern_name)
     traffic = None
     if tr is not None and tr.get("workload") == name:
         traffic = tr.get("dram_bytes_per_launch")
@@ -455,7 +505,8 @@ def run_gpu(args):
     ib = [idx, torch.empty_like(idx)]
     wb = [wt, torch.empty_like(wt)]
     ob = [out, torch.empty_like(out)]
-    rq = dict(recv_q=recv_q, recv_scales=recv_s) if fp8 else dict(recv=recv)
+    rq = dict(recv_q=recv_q, recv_scales=recv_s) if fp8 else (dict(recv_c=recv) if coal
+                                                                else dict(recv=recv))
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
     def e2e_run(n):
@@ -478,11 +529,18 @@ def run_gpu(args):
             if i >= 2:
                 stream.wait_event(d2h_done[i - 2])
             m.moe_layout(ib[b], E, R, workspace=ws, err_word=err, out=lay, stream=stream)
-            if fp8:
-                m.moe_dispatch_quant(xb[b], lay.slot_of, err_word=err, stream=stream, **rq)
+            if coal:
+                m.moe_layout_coalesced(ib[b], lay.slot_of, E, R, workspace=wsc, err_word=err,
+                                       out=co, stream=stream)
+                m.moe_dispatch_coalesced(xb[b], co.crow, rows, err_word=err, stream=stream, **rq)
+                m.moe_combine_coalesced(y, lay.slot_of, wb[b], co, rows, partial=partial,
+                                        out=ob[b], err_word=err, stream=stream)
             else:
-                m.moe_dispatch(xb[b], lay.slot_of, err_word=err, stream=stream, **rq)
-            m.moe_combine(y, lay.slot_of, wb[b], out=ob[b], err_word=err, stream=stream)
+                if fp8:
+                    m.moe_dispatch_quant(xb[b], lay.slot_of, err_word=err, stream=stream, **rq)
+                else:
+                    m.moe_dispatch(xb[b], lay.slot_of, err_word=err, stream=stream, **rq)
+                m.moe_combine(y, lay.slot_of, wb[b], out=ob[b], err_word=err, stream=stream)
             comp_done[i].record(stream)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(comp_done[i])
@@ -509,7 +567,7 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8-e4m3 + bf16" if fp8 else "bf16", "data": "synthetic",
         "config": {"workload": f"{name} T={T} H={H} k={k} E={E} R={R}",
-                   "tokens_per_step": T,
+                   "tokens_per_step": T, "variant": args.variant,
                    "l2": "flushed every step outside the events: 2xL2 written before layout+"
                          "dispatch, 2xL2 read before combine",
                    "parallelism": f"replicas x{world}"},
@@ -520,7 +578,8 @@ def run_gpu(args):
                      "duration_source": source},
         "segments_ms": {"layout+" + d_name: statistics.mean(t_front), "combine": avg_c},
         "kernels_ms": {"layout": statistics.mean(t_layout), d_name: avg_d, "combine": avg_c},
-        "step_hbm_gbs": step_bytes(T, H, k, E, R, fp8) / (ms_per_step / 1000.0) / 1e9,
+        "step_hbm_gbs": (None if coal else
+                         step_bytes(T, H, k, E, R, fp8) / (ms_per_step / 1000.0) / 1e9),
         "wall_ms_per_step_incl_flush": 1000.0 * wall / args.steps,
         "e2e": {"value": world * T / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -528,10 +587,12 @@ def run_gpu(args):
                 "how": "public API; H2D of step i+1 and D2H of step i-1 overlap step i's kernels "
                        "(three streams, double-buffered inputs/outputs); one step's footprint "
                        "exceeds L2"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (6 if coal else 3) * args.steps,
         "clocks": clocks.summary(),
     }
-    if not args.no_cpu_baseline and world == 1:
+    if coal:
+        line["config"]["coalesced_rows"] = {"N": N, "Nc": Nc}
+    if not args.no_cpu_baseline and world == 1 and not coal:
         line["cpu_baseline"] = cpu_baseline(name, args.cpu_budget)
     print(json.dumps(line), flush=True)
 
@@ -549,6 +610,8 @@ def main(argv=None):
     p.add_argument("--ref-tokens", type=int, default=64,
                    help="tokens per oracle step in --impl reference")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--variant", choices=["plain", "coalesced"], default="plain",
+                   help="plain: the hot path; coalesced: the rank-coalesced path (bf16)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
