@@ -19,9 +19,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_ep.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_BAD_INDEX, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, \
-    MOE_ERR_UNSUPPORTED = range(6)
+    MOE_ERR_UNSUPPORTED, MOE_ERR_INTEGRITY = range(7)
 MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
-MOE_ERRBIT_BAD_INDEX, MOE_ERRBIT_TIMEOUT = 0x1, 0x2
+MOE_ERRBIT_BAD_INDEX, MOE_ERRBIT_TIMEOUT, MOE_ERRBIT_SENTINEL, MOE_ERRBIT_CHECKSUM = 0x1, 0x2, 0x4, 0x8
+MOE_SYNC_WORD, MOE_SYNC_SENTINEL, MOE_SYNC_BATCH, MOE_SYNC_BARRIER = range(4)
 MOE_MAX_EXPERTS = 1024
 
 # Every symbol the header declares, with its ctypes signature.
@@ -36,7 +37,7 @@ SIGNATURES = {
     "moe_combine": ([_I, _I, _I, _P, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_read_error": ([_U32P, _I, _P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "moe_layout_noalloc": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
-    "moe_flag_words": ([_I, _I, _I], ctypes.c_size_t),
+    "moe_sync_words": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
     "moe_combine_backward": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_dispatch_backward": ([_I, _I, _I, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_layout_coalesced": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P],
@@ -44,8 +45,9 @@ SIGNATURES = {
     "moe_dispatch_coalesced": ([_I, _I, _I, _P, _P, _I, _P, _U32P, _P], ctypes.c_int),
     "moe_combine_coalesced": ([_I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _I, _U32P, _P],
                               ctypes.c_int),
-    "moe_dispatch_combine_flagged": ([_I, _I, _I, _P, _P, _P, _P, _P, _I, _P, ctypes.c_uint32,
-                                      ctypes.c_uint64, ctypes.c_int64, _U32P, _P], ctypes.c_int),
+    "moe_dispatch_combine_flagged": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P,
+                                      ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64, _U32P,
+                                      _P], ctypes.c_int),
 }
 
 
@@ -358,18 +360,36 @@ def moe_dispatch_backward(drecv: torch.Tensor, slot_of: torch.Tensor, *,
     return dx
 
 
-def moe_flag_words(T: int, H: int, k: int) -> int:
-    return int(_lib.moe_flag_words(T, H, k))
+def moe_sync_words(T: int, H: int, k: int, mode: int, block_bytes: int) -> int:
+    return int(_lib.moe_sync_words(T, H, k, mode, block_bytes))
 
 
-class FlagWords:
-    """Sequence words for moe_dispatch_combine_flagged: zero-filled once, and a
-    fresh epoch (1, 2, 3, ...) for every call that reuses them."""
+SENTINEL_WORD = -1  # every 32-bit word 0xFFFFFFFF (two bf16 0xFFFF NaNs)
 
-    def __init__(self, T: int, H: int, k: int, device=None):
-        self.words = torch.zeros(max(moe_flag_words(T, H, k), 1), dtype=torch.int32,
-                                 device=device or "cuda")
+
+class SyncState:
+    """What moe_dispatch_combine_flagged keeps between calls for one shape:
+    the readiness words (zero-filled once) with a fresh epoch per call and, for
+    MOE_SYNC_SENTINEL, recv and y filled with the sentinel."""
+
+    def __init__(self, T: int, H: int, k: int, mode: int = MOE_SYNC_WORD,
+                 block_bytes: int = 2048, device=None):
+        dev = device or "cuda"
+        n = moe_sync_words(T, H, k, mode, block_bytes)
+        if n == 0 and mode != MOE_SYNC_SENTINEL:
+            raise ValueError(f"invalid granularity {block_bytes} for mode {mode}")
+        self.mode, self.block_bytes = mode, block_bytes
+        self.words = torch.zeros(max(n, 2), dtype=torch.int32, device=dev)
         self.epoch = 0
+        self.recv = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+        if mode == MOE_SYNC_SENTINEL:
+            self.refill()
+
+    def refill(self) -> None:
+        """Sentinel-fill recv and y (needed again after a call that failed)."""
+        self.recv.view(torch.int16).fill_(SENTINEL_WORD)
+        self.y.view(torch.int16).fill_(SENTINEL_WORD)
 
     def next_epoch(self) -> int:
         self.epoch = (self.epoch % 0xFFFFFFFF) + 1
@@ -377,32 +397,32 @@ class FlagWords:
 
 
 def moe_dispatch_combine_flagged(x: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.Tensor,
-                                 flags: FlagWords, *, out_dtype: torch.dtype = torch.bfloat16,
-                                 recv: Optional[torch.Tensor] = None,
+                                 state: SyncState, *, out_dtype: torch.dtype = torch.bfloat16,
                                  out: Optional[torch.Tensor] = None,
                                  spin_limit_ns: int = 1_000_000_000, fault_skip_pair: int = -1,
                                  err_word: Optional[torch.Tensor] = None,
                                  stream: Optional[torch.cuda.Stream] = None):
-    """Dispatch, identity expert and combine in one persistent kernel with
-    per-row-chunk readiness words.  Returns (recv, out)."""
+    """Dispatch, identity expert and combine in one persistent kernel; the
+    expert and combine phases learn that rows have arrived through
+    `state.mode`.  Returns (recv, y, out)."""
     T, H = x.shape
     k = slot_of.shape[1]
     _want(x, "x", torch.bfloat16)
     _want(slot_of, "slot_of", torch.int32, (T, k))
     _want(topk_w, "topk_w", torch.float32, (T, k))
-    if recv is None:
-        recv = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
+    _want(state.recv, "recv", torch.bfloat16, (T * k, H))
+    _want(state.y, "y", torch.bfloat16, (T * k, H))
     if out is None:
         out = torch.empty((T, H), dtype=out_dtype, device=x.device)
-    _want(recv, "recv", torch.bfloat16, (T * k, H))
     _want(out, "out", out_dtype, (T, H))
     code = MOE_OUT_BF16 if out_dtype == torch.bfloat16 else MOE_OUT_F32
     _check(_lib.moe_dispatch_combine_flagged(T, H, k, _ptr(x), _ptr(slot_of), _ptr(topk_w),
-                                             _ptr(recv), _ptr(out), code, _ptr(flags.words),
-                                             flags.next_epoch(), int(spin_limit_ns),
+                                             _ptr(state.recv), _ptr(state.y), _ptr(out), code,
+                                             state.mode, state.block_bytes, _ptr(state.words),
+                                             state.next_epoch(), int(spin_limit_ns),
                                              int(fault_skip_pair), _ptr(err_word),
                                              _stream(stream)), "moe_dispatch_combine_flagged")
-    return recv, out
+    return state.recv, state.y, out
 
 
 def moe_read_error(err_word: torch.Tensor, clear: bool = True,
@@ -419,7 +439,7 @@ def moe_read_error(err_word: torch.Tensor, clear: bool = True,
 __all__ = [
     "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word", "new_workspace",
     "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
-    "moe_combine", "moe_read_error", "moe_flag_words", "FlagWords",
+    "moe_combine", "moe_read_error", "moe_sync_words", "SyncState",
     "moe_combine_backward", "moe_dispatch_backward",
     "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_combine_coalesced",
     "moe_dispatch_combine_flagged", "LIB_PATH", "SIGNATURES",

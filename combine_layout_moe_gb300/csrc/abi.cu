@@ -56,7 +56,7 @@ bool pairs_ok(int T, int k)
 
 extern "C" {
 
-int moe_abi_version(void) { return 1; }
+int moe_abi_version(void) { return 2; }
 
 const char *moe_status_string(int status)
 {
@@ -73,6 +73,8 @@ const char *moe_status_string(int status)
         return "device-side wait timed out";
     case MOE_ERR_UNSUPPORTED:
         return "unsupported configuration";
+    case MOE_ERR_INTEGRITY:
+        return "payload equals the sentinel, or a checksum does not match the data";
     default:
         return "unknown status";
     }
@@ -248,33 +250,41 @@ moe_status moe_dispatch_backward(int T, int H, int k, const void *drecv, const i
                                          out_dtype == MOE_OUT_F32, err_word, stream));
 }
 
-size_t moe_flag_words(int T, int H, int k)
+size_t moe_sync_words(int T, int H, int k, int mode, int block_bytes)
 {
     if (!pairs_ok(T, k) || H < 8 || H % 8 != 0)
         return 0;
-    return (size_t)T * k * (size_t)moe::flagged_chunks(H);
+    return moe::sync_words(T, H, k, mode, block_bytes);
 }
 
 moe_status moe_dispatch_combine_flagged(int T, int H, int k, const void *x, const int32_t *slot_of,
-                                        const float *topk_w, void *recv, void *out, int out_dtype,
-                                        uint32_t *seq, uint32_t epoch, uint64_t spin_limit_ns,
+                                        const float *topk_w, void *recv, void *y, void *out,
+                                        int out_dtype, int mode, int block_bytes, uint32_t *words,
+                                        uint32_t epoch, uint64_t spin_limit_ns,
                                         int64_t fault_skip_pair, uint32_t *err_word,
                                         cudaStream_t stream)
 {
-    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0 || epoch == 0 || spin_limit_ns == 0)
+    if (!pairs_ok(T, k) || H < 8 || H % 8 != 0 || spin_limit_ns == 0)
+        return MOE_ERR_INVALID_ARG;
+    if (mode < MOE_SYNC_WORD || mode > MOE_SYNC_BARRIER ||
+        !moe::sync_granularity_ok(mode, H, block_bytes))
+        return MOE_ERR_INVALID_ARG;
+    if ((mode == MOE_SYNC_WORD || mode == MOE_SYNC_BATCH) && epoch == 0)
         return MOE_ERR_INVALID_ARG;
     if (k > 32)
         return MOE_ERR_UNSUPPORTED;
     if (out_dtype != MOE_OUT_BF16 && out_dtype != MOE_OUT_F32)
         return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!x || !slot_of || !topk_w || !recv || !out || !seq))
+    const bool need_words = moe::sync_words(T, H, k, mode, block_bytes) > 0;
+    if (T > 0 && (!x || !slot_of || !topk_w || !recv || !y || !out || (need_words && !words)))
         return MOE_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(out, 16) || !aligned(slot_of, 4) ||
-        !aligned(topk_w, 4) || !aligned(seq, 4) || !aligned(err_word, 4))
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(y, 16) || !aligned(out, 16) ||
+        !aligned(slot_of, 4) || !aligned(topk_w, 4) || !aligned(words, 8) ||
+        !aligned(err_word, 4))
         return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_dispatch_combine_flagged(
-        T, H, k, x, slot_of, topk_w, recv, out, out_dtype == MOE_OUT_F32, seq, epoch, spin_limit_ns,
-        fault_skip_pair, err_word, stream));
+        T, H, k, x, slot_of, topk_w, recv, y, out, out_dtype == MOE_OUT_F32, mode, block_bytes,
+        words, epoch, spin_limit_ns, fault_skip_pair, err_word, stream));
 }
 
 moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t stream, uint32_t *bits_out)
@@ -297,6 +307,8 @@ moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t stream, ui
         return MOE_ERR_TIMEOUT;
     if (bits & MOE_ERRBIT_BAD_INDEX)
         return MOE_ERR_BAD_INDEX;
+    if (bits & (MOE_ERRBIT_SENTINEL | MOE_ERRBIT_CHECKSUM))
+        return MOE_ERR_INTEGRITY;
     return MOE_OK;
 }
 

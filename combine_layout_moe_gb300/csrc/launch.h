@@ -45,14 +45,16 @@ cudaError_t launch_combine_backward(int T, int H, int k, const void *dout, const
                                     const int32_t *slot_of, const float *topk_w, void *dy,
                                     float *dw, uint32_t *err_word, cudaStream_t stream);
 
-int flagged_chunks(int H);
+bool sync_granularity_ok(int mode, int H, int G);
+
+size_t sync_words(int T, int H, int k, int mode, int G);
 
 cudaError_t launch_dispatch_combine_flagged(int T, int H, int k, const void *x,
                                             const int32_t *slot_of, const float *topk_w,
-                                            void *recv, void *out, bool out_f32, uint32_t *seq,
-                                            uint32_t epoch, uint64_t spin_limit_ns,
-                                            int64_t skip_pair, uint32_t *err_word,
-                                            cudaStream_t stream);
+                                            void *recv, void *y, void *out, bool out_f32,
+                                            int mode, int G, uint32_t *words, uint32_t epoch,
+                                            uint64_t spin_limit_ns, int64_t skip_pair,
+                                            uint32_t *err_word, cudaStream_t stream);
 
 // Launches `kernel` on `stream` with programmatic stream serialisation, so it
 // may become resident while the previous kernel in the stream is still running

@@ -47,7 +47,9 @@ typedef enum moe_status {
     MOE_ERR_BAD_INDEX = 2,   /* device saw an expert id or slot out of range      */
     MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed              */
     MOE_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up                */
-    MOE_ERR_UNSUPPORTED = 5  /* well-formed request outside this build's limits   */
+    MOE_ERR_UNSUPPORTED = 5, /* well-formed request outside this build's limits   */
+    MOE_ERR_INTEGRITY = 6    /* payload equal to the sentinel, or a checksum that */
+                             /* does not match the data                           */
 } moe_status;
 
 typedef enum moe_out_dtype { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 } moe_out_dtype;
@@ -55,6 +57,16 @@ typedef enum moe_out_dtype { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 } moe_out_dtype;
 /* bits OR-ed into *err_word by the kernels */
 #define MOE_ERRBIT_BAD_INDEX 0x1u
 #define MOE_ERRBIT_TIMEOUT 0x2u
+#define MOE_ERRBIT_SENTINEL 0x4u
+#define MOE_ERRBIT_CHECKSUM 0x8u
+
+/* how moe_dispatch_combine_flagged's readers learn that data has arrived */
+typedef enum moe_sync_mode {
+    MOE_SYNC_WORD = 0,     /* a 32-bit word per (row, block), set after a fence     */
+    MOE_SYNC_SENTINEL = 1, /* the reader polls the data itself (sentinel-filled)   */
+    MOE_SYNC_BATCH = 2,    /* a 64-bit (epoch, checksum) word per (row, batch)      */
+    MOE_SYNC_BARRIER = 3   /* a grid barrier between the phases (stop-and-wait)     */
+} moe_sync_mode;
 
 /* largest expert count the layout kernels hold in shared memory */
 #define MOE_MAX_EXPERTS 1024
@@ -289,35 +301,69 @@ MOE_API moe_status moe_combine_coalesced(int T, int H, int k, const void *y,
 
 /*
  * moe_dispatch_combine_flagged -- dispatch, an identity expert and combine in
- * one persistent kernel, with Data-as-Flag readiness instead of a barrier.
+ * one persistent kernel, each hop synchronised by the reader observing the
+ * data's readiness instead of a kernel boundary.
  *
- * UBEP, section 3.4 (Data-as-Flag: readiness travels with the data), section
- * 3.2 (consumers start as soon as their inputs are signalled) and section 6
- * (without atomic 512-byte writes, fall back to explicit fences).  Producers
- * copy each token's row chunk to its k slots, fence, and set one 32-bit
- * sequence word per (slot row, chunk) to `epoch`; consumers wait for the words
- * of a token's k rows (acquire loads, bounded by spin_limit_ns), read the rows
- * back and reduce them as moe_combine does.  Results: recv as moe_dispatch,
- * out = moe_combine(recv, slot_of, topk_w) (the identity expert).
+ * UBEP, section 3.4 and Figure 6 (Data-as-Flag: Token-Flag Fusion,
+ * Data-for-Checksum, Sentinel Polling), section 3.2 (consumers start as soon
+ * as their inputs are signalled) and section 6 (without atomic 512-byte
+ * writes, fall back to explicit fences).  Three phases per warp, in one
+ * cooperative launch:
+ *   produce  recv[slot_of[t, j]] = x[t]                     (token order)
+ *   expert   y[s] = recv[s], the identity expert     (receive-row order)
+ *   combine  out[t] = sum_j w[t, j] * y[slot_of[t, j]]      (token order),
+ *            fp32 fused multiply-adds in slot order from +0, one rounding
+ * The expert and combine phases read rows written by other SMs; how they know
+ * the rows have arrived is `mode`, at granularity `block_bytes` (G):
+ *   MOE_SYNC_WORD      a 32-bit word per (row, G-byte block) per hop, set to
+ *                      `epoch` after a fence; G in {16, 32, ..., 512} or a
+ *                      multiple of 512
+ *   MOE_SYNC_SENTINEL  no words.  recv and y must hold 0xFFFFFFFF in every
+ *                      32-bit word before the call (memset 0xFF); readers
+ *                      poll the data until no word is the sentinel and write
+ *                      it back after use, so a call that succeeds leaves them
+ *                      ready for the next.  After a call that reports an
+ *                      error, refill both.  A payload word equal to the
+ *                      sentinel (two bf16 0xFFFF NaNs) sets
+ *                      MOE_ERRBIT_SENTINEL.  G is ignored (every word is
+ *                      checked) but must still be valid as for WORD
+ *   MOE_SYNC_BATCH     a 64-bit (epoch, checksum) word per (row, G-byte
+ *                      batch) per hop, G a multiple of 512; the checksum is
+ *                      the sum of the first 32-bit word of each 512-byte
+ *                      block, and a reader that finds a different sum sets
+ *                      MOE_ERRBIT_CHECKSUM
+ *   MOE_SYNC_BARRIER   no readiness: a grid barrier between the phases
  *
- *   seq       moe_flag_words(T, H, k) uint32 device words, zero-filled once;
- *             none may already hold `epoch`
- *   epoch     non-zero and different on every call that reuses `seq`
- *             (e.g. 1, 2, 3, ...)
- *   spin_limit_ns   bound on each wait; a wait that runs out sets
- *             MOE_ERRBIT_TIMEOUT, that token chunk's output is left unwritten,
- *             and the kernel still returns
+ *   x        [T, H]    bf16 token rows
+ *   slot_of  [T, k]    from moe_layout
+ *   topk_w   [T, k]    fp32 router weights
+ *   recv, y  [T*k, H]  bf16: the dispatched rows and the expert's output
+ *   out      [T, H]    bf16 (MOE_OUT_BF16) or fp32 (MOE_OUT_F32)
+ *   words    moe_sync_words(T, H, k, mode, block_bytes) uint32 device words,
+ *            zero-filled once (may be NULL when that is 0); WORD and BATCH:
+ *            none may already hold `epoch`
+ *   epoch    non-zero and different on every call that reuses `words`
+ *            (WORD and BATCH)
+ *   spin_limit_ns   bound on each expert-phase wait; combine-phase waits get
+ *            three times as long (one may sit behind an expert wait that ran
+ *            out).  A wait that runs out sets MOE_ERRBIT_TIMEOUT and leaves
+ *            that unit unwritten; the warp then stops waiting for data that
+ *            is not already there, and the kernel returns
  *   fault_skip_pair test hook: the producer of pair t*k+j == fault_skip_pair
- *             does not set its word, so the matching consumer's wait runs out;
- *             pass -1 in normal use
+ *            publishes nothing for it (WORD, BATCH) or does not write it
+ *            (SENTINEL), so the readers of that row time out; -1 in normal
+ *            use, ignored by BARRIER
  *
- * One cooperative launch (every CTA resident).  1 <= k <= 32; H % 8 == 0.
+ * Results: recv = moe_dispatch(x, slot_of) and y = recv (WORD, BATCH,
+ * BARRIER; SENTINEL leaves both sentinel-filled), out = moe_combine(y,
+ * slot_of, topk_w).  1 <= k <= 32 (larger k: MOE_ERR_UNSUPPORTED); H % 8 == 0.
  */
-MOE_API size_t moe_flag_words(int T, int H, int k);
+MOE_API size_t moe_sync_words(int T, int H, int k, int mode, int block_bytes);
 
 MOE_API moe_status moe_dispatch_combine_flagged(int T, int H, int k, const void *x,
                                         const int32_t *slot_of, const float *topk_w,
-                                        void *recv, void *out, int out_dtype, uint32_t *seq,
+                                        void *recv, void *y, void *out, int out_dtype,
+                                        int mode, int block_bytes, uint32_t *words,
                                         uint32_t epoch, uint64_t spin_limit_ns,
                                         int64_t fault_skip_pair, uint32_t *err_word,
                                         cudaStream_t stream);

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(m):
 
 
 def test_status_strings_and_version(m):
-    assert m.moe_abi_version() == 1
+    assert m.moe_abi_version() == 2
     assert m.moe_status_string(0) == "ok"
     assert "range" in m.moe_status_string(m.MOE_ERR_BAD_INDEX)
     assert m.moe_status_string(99) == "unknown status"
@@ -96,14 +96,25 @@ def test_payload_calls_reject_bad_shapes_and_alignment(m):
     assert L.moe_combine(4, 64, 2, FAKE, FAKE, FAKE, FAKE + 8, 0, None, None) == bad
     assert L.moe_combine(4, 64, 0, FAKE, FAKE, FAKE, FAKE, 0, None, None) == bad
     assert L.moe_read_error(None, 1, None, None) == bad
-    # flagged variant: epoch 0, zero spin limit, k above 32
-    assert L.moe_dispatch_combine_flagged(4, 64, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 10,
-                                          -1, None, None) == bad
-    assert L.moe_dispatch_combine_flagged(4, 64, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 0,
-                                          -1, None, None) == bad
-    assert L.moe_dispatch_combine_flagged(4, 64, 40, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 10,
-                                          -1, None, None) == m.MOE_ERR_UNSUPPORTED
-    assert m.moe_flag_words(1024, 7168, 8) == 1024 * 8 * 7
+    # flagged variant: (mode, granularity, epoch, spin limit) -> status
+    def flagged(k, mode, G, epoch, spin):
+        return L.moe_dispatch_combine_flagged(4, 64, k, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0,
+                                              mode, G, FAKE, epoch, spin, -1, None, None)
+    assert flagged(2, m.MOE_SYNC_WORD, 512, 0, 10) == bad               # epoch 0
+    assert flagged(2, m.MOE_SYNC_WORD, 512, 1, 0) == bad                # no spin limit
+    assert flagged(2, m.MOE_SYNC_WORD, 48, 1, 10) == bad                # 48 does not divide 512
+    assert flagged(2, m.MOE_SYNC_WORD, 1000, 1, 10) == bad              # not a multiple of 512
+    assert flagged(2, m.MOE_SYNC_BATCH, 256, 1, 10) == bad              # batches of whole blocks
+    assert flagged(2, 4, 512, 1, 10) == bad                             # no such mode
+    assert flagged(40, m.MOE_SYNC_WORD, 512, 1, 10) == m.MOE_ERR_UNSUPPORTED
+    # words per mode: two hops x rows x blocks (BATCH: 64-bit words)
+    T, H, k = 1024, 7168, 8
+    assert m.moe_sync_words(T, H, k, m.MOE_SYNC_WORD, 2048) == 2 * T * k * 7
+    assert m.moe_sync_words(T, H, k, m.MOE_SYNC_WORD, 32) == 2 * T * k * 448
+    assert m.moe_sync_words(T, H, k, m.MOE_SYNC_BATCH, 4096) == 4 * T * k * 4
+    assert m.moe_sync_words(T, H, k, m.MOE_SYNC_BARRIER, 512) == 2
+    assert m.moe_sync_words(T, H, k, m.MOE_SYNC_SENTINEL, 512) == 0
+    assert m.moe_sync_words(T, H, k, m.MOE_SYNC_WORD, 24) == 0
     # backward: k above 32, dw without y, bad output dtype
     assert L.moe_combine_backward(4, 64, 40, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
                                   None) == m.MOE_ERR_UNSUPPORTED
