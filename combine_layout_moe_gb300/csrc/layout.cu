@@ -31,7 +31,11 @@ namespace moe {
 
 constexpr int LAYOUT_THREADS = 512;
 constexpr int LAYOUT_WARPS = LAYOUT_THREADS / 32;
-constexpr int LAYOUT_TARGET_TILE = 2048;  // pairs per CTA while the tile count is small
+// Tunable (compile-time; the default is the shipped configuration).
+#ifndef MOE_LAYOUT_TARGET_TILE
+#define MOE_LAYOUT_TARGET_TILE 1024
+#endif
+constexpr int LAYOUT_TARGET_TILE = MOE_LAYOUT_TARGET_TILE;  // pairs per CTA while tiles are few
 constexpr int LAYOUT_MAX_TILES = 128;     // bounds the tile-count table each CTA reads
 constexpr int LAYOUT_BATCH = 8;           // expert ids loaded ahead per lane
 constexpr int TABLE_UNROLL = 8;           // independent table loads in flight per thread
@@ -158,22 +162,36 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
         report(err_word, MOE_ERRBIT_BAD_INDEX);
     __syncthreads();
     LAYOUT_TRACE(1);
-    for (int e = tid; e < E; e += LAYOUT_THREADS) {
-        int32_t s = 0;
+    if (tiles == 1) {
+        // one tile: the totals are this CTA's own counts, and no tile comes
+        // before it (pre stays 0); no table, no grid barrier
+        for (int e = tid; e < E; e += LAYOUT_THREADS) {
+            int32_t s = 0;
 #pragma unroll 4
-        for (int w = 0; w < LAYOUT_WARPS; ++w)
-            s += wcnt[w * E + e];
-        tile_counts[(int64_t)blockIdx.x * E + e] = s;
+            for (int w = 0; w < LAYOUT_WARPS; ++w)
+                s += wcnt[w * E + e];
+            offs[e] = s;
+        }
+        LAYOUT_TRACE(2);
+        LAYOUT_TRACE(3);
+    } else {
+        for (int e = tid; e < E; e += LAYOUT_THREADS) {
+            int32_t s = 0;
+#pragma unroll 4
+            for (int w = 0; w < LAYOUT_WARPS; ++w)
+                s += wcnt[w * E + e];
+            tile_counts[(int64_t)blockIdx.x * E + e] = s;
+        }
+
+        LAYOUT_TRACE(2);
+        // 2. every tile row is written
+        if (!grid_barrier(barrier, err_word))
+            return;
+        LAYOUT_TRACE(3);
     }
 
-    LAYOUT_TRACE(2);
-    // 2. every tile row is written
-    if (!grid_barrier(barrier, err_word))
-        return;
-    LAYOUT_TRACE(3);
-
     // 3a. column sums of the table; thread (part, e) sums rows part, part+P, ...
-    {
+    if (tiles > 1) {
         const int P = E >= LAYOUT_THREADS ? 1 : LAYOUT_THREADS / E;
         const int part = tid / E;
         for (int e = tid % E; part < P && e < E; e += LAYOUT_THREADS) {

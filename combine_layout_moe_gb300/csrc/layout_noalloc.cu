@@ -3,8 +3,8 @@
 // Some callers cannot allocate device memory when they call the layout: code
 // handed fixed buffers by a host framework that owns all allocation, or
 // runtimes that forbid cudaMalloc once they have started.  They cannot supply
-// moe_layout's workspace.  This variant runs the same two layout kernels, with
-// their per-tile count table in a fixed array compiled into the library
+// moe_layout's workspace.  This variant runs the same layout kernel, with
+// its per-tile count table in a fixed array compiled into the library
 // instead of a caller workspace.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
