@@ -151,7 +151,12 @@ __global__ void __launch_bounds__(32)
 
 constexpr int DISPATCH_THREADS = 256;
 constexpr int DISPATCH_U = 4;  // 16-byte vectors per lane per item
-constexpr int QUANT_U = 2;     // 16-lane quantisation blocks per half-warp per item
+// 16-lane quantisation blocks per half-warp per item (compile-time tunable;
+// the default is the shipped configuration)
+#ifndef MOE_QUANT_U
+#define MOE_QUANT_U 2
+#endif
+constexpr int QUANT_U = MOE_QUANT_U;
 
 template <int U>
 __global__ void __launch_bounds__(DISPATCH_THREADS)

@@ -42,13 +42,16 @@ constexpr int TABLE_UNROLL = 8;           // independent table loads in flight p
 constexpr size_t LAYOUT_BARRIER_BYTES = 256;  // workspace head: grid-barrier count and generation
 
 // Out-of-span lanes carry NO_PAIR; pairs with an expert id outside [0, E) carry
-// BAD_PAIR (they get slot -1 and take no slot).
+// BAD_PAIR (they get slot -1 and take no slot).  With COAL, a pair whose rank
+// an earlier slot j' of its token already chose carries SHARED_PAIR - j': it
+// takes no row of its own and shares slot j''s.
 constexpr int NO_PAIR = -1;
 constexpr int BAD_PAIR = -2;
+constexpr int SHARED_PAIR = -3;
 
 // Key of pair i: its expert id, or (COAL) its destination rank when it is the
-// first slot of its token that chose that rank, else NO_PAIR (it takes no
-// row).  Ids outside [0, E) give BAD_PAIR.
+// first slot of its token that chose that rank (else SHARED_PAIR - that
+// slot).  Ids outside [0, E) give BAD_PAIR.
 template <bool COAL>
 __device__ __forceinline__ int pair_key(const int32_t *__restrict__ idx, int64_t i, int E, int El,
                                         int k)
@@ -63,7 +66,7 @@ __device__ __forceinline__ int pair_key(const int32_t *__restrict__ idx, int64_t
     for (int jj = 0; jj < j; ++jj) {
         const int e2 = ld_nc_s32(idx + i - j + jj);
         if ((unsigned)e2 < (unsigned)E && e2 / El == r)
-            return NO_PAIR;
+            return SHARED_PAIR - jj;
     }
     return r;
 }
@@ -121,7 +124,8 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
                   int tiles, unsigned *barrier, int32_t *tile_counts,
                   int32_t *__restrict__ expert_counts, int32_t *__restrict__ expert_offsets,
                   int32_t *__restrict__ rank_offsets, int32_t *__restrict__ slot_of,
-                  int32_t *__restrict__ src_of, uint32_t *err_word)
+                  int32_t *__restrict__ src_of, const int32_t *__restrict__ plain_slot,
+                  int32_t *__restrict__ expand, uint32_t *err_word)
 {
     extern __shared__ int32_t smem[];
     int32_t *wcnt = smem;                     // [LAYOUT_WARPS][E]: counts, then cursors
@@ -292,12 +296,34 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
             const int64_t i = first + b * 32 + lane;
             const int e = ev[b];
             const unsigned peers = warp_peers<NBITS>(e);
+            int32_t s = -1;
             if (e >= 0) {
-                const int32_t s = cur[e] + __popc(peers & lt);
+                s = cur[e] + __popc(peers & lt);
                 slot_of[i] = s;
                 src_of[s] = (int32_t)i;
+                if (COAL && plain_slot != nullptr) {
+                    // an owner maps its plain slot to its own row here; the
+                    // shared pairs do it below, after the shuffle
+                    const int32_t ps = ld_nc_s32(plain_slot + i);
+                    if ((unsigned)ps < (unsigned)N)
+                        expand[ps] = s;
+                }
             } else if (e == BAD_PAIR) {
                 slot_of[i] = -1;
+            }
+            if (COAL && plain_slot != nullptr) {
+                // k divides 32, so this step starts a token and holds whole
+                // tokens: a shared pair takes its row from the lane of the
+                // slot that owns it and maps its plain slot to that row
+                const int j = lane % k;
+                const int oj = e <= SHARED_PAIR ? SHARED_PAIR - e : j;
+                const int32_t c = __shfl_sync(FULL_MASK, s, lane - j + oj);
+                if (e <= SHARED_PAIR) {
+                    slot_of[i] = c;
+                    const int32_t ps = ld_nc_s32(plain_slot + i);
+                    if ((unsigned)ps < (unsigned)N)
+                        expand[ps] = c;
+                }
             }
             __syncwarp();
             if (e >= 0 && (peers & lt) == 0)
@@ -351,8 +377,8 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, 
                                    const int32_t *topk_idx, unsigned *barrier,
                                    int32_t *tile_counts, int32_t *expert_counts,
                                    int32_t *expert_offsets, int32_t *rank_offsets,
-                                   int32_t *slot_of, int32_t *src_of, uint32_t *err_word,
-                                   cudaStream_t stream)
+                                   int32_t *slot_of, int32_t *src_of, const int32_t *plain_slot,
+                                   int32_t *expand, uint32_t *err_word, cudaStream_t stream)
 {
     const size_t smem = layout_smem(E);
     cudaError_t e = cudaSuccess;
@@ -378,25 +404,28 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, 
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS, COAL>, topk_idx, N, E, R, e_real, El, k,
                            p.span, p.tiles, barrier, tile_counts, expert_counts, expert_offsets,
-                           rank_offsets, slot_of, src_of, err_word);
+                           rank_offsets, slot_of, src_of, plain_slot, expand, err_word);
     if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
         // the driver refused the attribute pair: launch cooperatively only
         (void)cudaGetLastError();
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS, COAL>, topk_idx, N, E, R, e_real, El, k,
                                p.span, p.tiles, barrier, tile_counts, expert_counts,
-                               expert_offsets, rank_offsets, slot_of, src_of, err_word);
+                               expert_offsets, rank_offsets, slot_of, src_of, plain_slot,
+                               expand, err_word);
     }
     return e;
 }
 
 // Count / scan / slot map over keys in [0, K): expert ids (COAL false) or the
-// destination ranks of owner pairs (COAL true).
+// destination ranks of owner pairs (COAL true; with plain_slot, the shared
+// pairs and the expand map are resolved in the same launch).
 template <bool COAL>
 static cudaError_t launch_keys(int T, int k, int K, int R, int e_real, int El,
                                const int32_t *topk_idx, int32_t *counts, int32_t *offsets,
                                int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
-                               void *workspace, uint32_t *err_word, cudaStream_t stream)
+                               const int32_t *plain_slot, int32_t *expand, void *workspace,
+                               uint32_t *err_word, cudaStream_t stream)
 {
     const int64_t N = (int64_t)T * k;
     if (N == 0) {
@@ -419,7 +448,7 @@ static cudaError_t launch_keys(int T, int k, int K, int R, int e_real, int El,
     case B:                                                                                    \
         return launch_layout_t<B, COAL>(N, K, R, e_real, El, k, p, topk_idx, barrier,          \
                                         tile_counts, counts, offsets, rank_offsets, slot_of,   \
-                                        src_of, err_word, stream);
+                                        src_of, plain_slot, expand, err_word, stream);
         MOE_LAYOUT_CASE(0)
         MOE_LAYOUT_CASE(1)
         MOE_LAYOUT_CASE(2)
@@ -443,7 +472,8 @@ cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
                           void *workspace, uint32_t *err_word, cudaStream_t stream)
 {
     return launch_keys<false>(T, k, E, R, E, E / R, topk_idx, expert_counts, expert_offsets,
-                              rank_offsets, slot_of, src_of, workspace, err_word, stream);
+                              rank_offsets, slot_of, src_of, nullptr, nullptr, workspace,
+                              err_word, stream);
 }
 
 // Non-owner slots take their owner's coalesced row; expand[slot_of[i]] = crow[i].
@@ -484,11 +514,16 @@ cudaError_t launch_layout_coalesced(int T, int k, int E, int R, const int32_t *t
                                     int32_t *expand, void *workspace, uint32_t *err_word,
                                     cudaStream_t stream)
 {
+    // When k divides 32 every 32-pair warp step holds whole tokens, and the
+    // layout kernel resolves shared pairs and the expand map itself;
+    // otherwise a second pass does.
+    const bool fused = 32 % k == 0;
     cudaError_t e = launch_keys<true>(T, k, R, R, E, E / R, topk_idx, rank_counts_c,
-                                      rank_offsets_c, nullptr, crow, src_pair_c, workspace,
-                                      err_word, stream);
+                                      rank_offsets_c, nullptr, crow, src_pair_c,
+                                      fused ? slot_of : nullptr, fused ? expand : nullptr,
+                                      workspace, err_word, stream);
     const int64_t N = (int64_t)T * k;
-    if (e != cudaSuccess || N == 0)
+    if (e != cudaSuccess || N == 0 || fused)
         return e;
     const int threads = 256;
     int64_t blocks = (N + threads - 1) / threads;

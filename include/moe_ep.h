@@ -239,8 +239,9 @@ MOE_API moe_status moe_dispatch_backward(int T, int H, int k, const void *drecv,
  *                  workspace concurrently)
  *
  * Ids outside [0, E) set MOE_ERRBIT_BAD_INDEX, get crow -1 and no row.
- * 1 <= R <= E <= MOE_MAX_EXPERTS, E % R == 0.  Two launches: the row map over
- * owners, then a pass that resolves the other slots and expand.
+ * 1 <= R <= E <= MOE_MAX_EXPERTS, E % R == 0.  One launch when k divides 32
+ * (every 32-pair warp step then holds whole tokens, so the other slots and
+ * expand are resolved in the same pass); otherwise a second launch does that.
  */
 MOE_API moe_status moe_layout_coalesced(int T, int k, int E, int R, const int32_t *topk_idx,
                                 const int32_t *slot_of, int32_t *rank_counts_c,
