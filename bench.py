@@ -62,9 +62,8 @@ def kernel_bytes(name: str, T: int, H: int, k: int, E: int, R: int = 1) -> int:
     combine        reads k rows per token, slot_of and weights, writes one row
     The coalesced kernels also depend on Nc, the number of coalesced rows:
     dispatch_coalesced  reads x and crow, writes Nc rows
-    combine_coalesced   pre-reduction: reads k rows per token, slot_of, weights
-                        and crow, writes Nc rows; then reads the Nc rows and
-                        crow, writes one row per token
+    combine_coalesced   reads k rows per token, slot_of, weights and crow,
+                        writes the Nc pre-reduced rows and one row per token
     """
     N = T * k
     if name == "layout_count":
@@ -85,7 +84,7 @@ def coalesced_bytes(name: str, T: int, H: int, k: int, Nc: int) -> int:
     if name == "dispatch_coalesced":
         return 2 * T * H + 4 * N + 2 * Nc * H
     if name == "combine_coalesced":
-        return (2 * N * H + 12 * N + 2 * Nc * H) + (2 * Nc * H + 4 * N + 2 * T * H)
+        return 2 * N * H + 12 * N + 2 * Nc * H + 2 * T * H
     raise KeyError(name)
 
 
@@ -469,9 +468,7 @@ def run_gpu(args):
     t_disp = [e[1].elapsed_time(e[2]) for e in evs]
 
     # roofline of the dominant kernel: combine is timed alone inside the timed
-    # steps; dispatch (when it dominates) in the breakdown pass.  In the
-    # coalesced variant the combine segment is its two launches (pre-reduction
-    # and per-token sum), measured together.
+    # steps; dispatch (when it dominates) in the breakdown pass.
     d_name = "dispatch_fp8" if fp8 else ("dispatch_coalesced" if coal else "dispatch_bf16")
     c_name = "combine_coalesced" if coal else "combine"
     avg_d, avg_c = statistics.mean(t_disp), statistics.mean(t_comb)
@@ -485,7 +482,7 @@ def run_gpu(args):
     kern_name = {"dispatch_bf16": "dispatch_bulk_kernel", "dispatch_fp8": "dispatch_fp8_kernel",
                  "combine": "combine_bulk_kernel",
                  "dispatch_coalesced": "dispatch_bulk_kernel<coalesced>",
-                 "combine_coalesced": "combine_bulk_kernel<pre> + combine_bulk_kernel<post>"}[dom]
+                 "combine_coalesced": "combine_bulk_kernel<coalesced>"}[dom]
     tr = None if coal else recorded_traffic(kern_name)
     traffic = None
     if tr is not None and tr.get("workload") == name:
@@ -587,7 +584,9 @@ def run_gpu(args):
                 "how": "public API; H2D of step i+1 and D2H of step i-1 overlap step i's kernels "
                        "(three streams, double-buffered inputs/outputs); one step's footprint "
                        "exceeds L2"},
-        "gpu_launches": (6 if coal else 3) * args.steps,
+        # layout, dispatch, combine; the coalesced step adds the coalesced
+        # layout (a second launch when k does not divide 32)
+        "gpu_launches": ((4 if 32 % k == 0 else 5) if coal else 3) * args.steps,
         "clocks": clocks.summary(),
     }
     if coal:

@@ -179,22 +179,44 @@ __device__ __forceinline__ void advance(int64_t &t, int &c, int step, int nchunk
     } while (0)
 #endif
 
+// Stores eight fp32 accumulators at element e0 of out: fp32, or rounded once
+// to bf16 (nearest-even).
+__device__ __forceinline__ void store_row8(void *out, int out_f32, int64_t e0, const float (&a)[8])
+{
+    if (out_f32) {
+        float *o = static_cast<float *>(out) + e0;
+        st_v4(o, make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                            __float_as_uint(a[3])));
+        st_v4(o + 4, make_uint4(__float_as_uint(a[4]), __float_as_uint(a[5]),
+                                __float_as_uint(a[6]), __float_as_uint(a[7])));
+    } else {
+        uint32_t rr[4];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(a[2 * hh], a[2 * hh + 1]);
+            rr[hh] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+        st_v4(static_cast<__nv_bfloat16 *>(out) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
+    }
+}
+
 // What a unit (token t, chunk c) of the bulk combine reduces.
 //   CB_PLAIN  out[t] from slots slot_of[t, :], weights topk_w[t, :] (null: 1)
-//   CB_PRE    the rank-side pre-reduction of the coalesced combine: the token's
-//             slots are grouped by coalesced row crow[t, :]; each group's
-//             weighted sum goes to out[crow] (bf16), groups led by their first
-//             slot, members folded in increasing j
-//   CB_POST   out[t] from the token's distinct coalesced rows crow[t, :] (each
-//             once, at its first slot), unit weights
-enum { CB_PLAIN = 0, CB_PRE = 1, CB_POST = 2 };
+//   CB_COAL   the coalesced combine in one pass: the token's slots are grouped
+//             by coalesced row crow[t, :]; each group's weighted sum (members
+//             folded in increasing j) is rounded to bf16 and stored to
+//             part[crow] -- the rank-side pre-reduction -- and out[t] is the
+//             fp32 sum of those rounded rows in order of their first slot --
+//             the token-side sum
+enum { CB_PLAIN = 0, CB_COAL = 1 };
 
 template <int KMAX, int MODE>
 __global__ void __launch_bounds__(CT_THREADS, 1)
     combine_bulk_kernel(const uint8_t *__restrict__ y, const int32_t *__restrict__ slot_of,
                         const float *__restrict__ topk_w, const int32_t *__restrict__ crow,
-                        void *__restrict__ out, int out_f32, int T, int H, int k, int bound,
-                        int gbound, int CH, int nchunks, int64_t units, uint32_t *err_word)
+                        void *__restrict__ part, void *__restrict__ out, int out_f32, int T,
+                        int H, int k, int bound, int gbound, int CH, int nchunks, int64_t units,
+                        uint32_t *err_word)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t bars = smem_addr(smem);
@@ -231,24 +253,14 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         int64_t t = u0 / nchunks;
         int c = (int)(u0 - t * nchunks);
         const bool kl = lane < k;
-        const unsigned kmask = k >= 32 ? FULL_MASK : (1u << k) - 1u;
         // this lane's slot of token `row`: source row, weight, whether it takes
-        // part, and (CB_PRE) its group's output row (called by the whole warp)
+        // part, and (CB_COAL) its coalesced row
         auto row_info = [&](int64_t row, int32_t &slot, float &w, bool &want, int32_t &grp) {
-            grp = 0;
-            if (MODE == CB_POST) {
-                slot = kl ? ld_nc_s32(crow + row * k + lane) : 0;
-                w = 1.0f;
-                const unsigned same = __match_any_sync(FULL_MASK, slot) & kmask;
-                want = kl && (same & lanemask_lt()) == 0;
-            } else {
-                slot = kl ? ld_nc_s32(slot_of + row * k + lane) : 0;
-                // a null weight array means unit weights (the gradient of dispatch)
-                w = kl ? (topk_w ? ld_nc_f32(topk_w + row * k + lane) : 1.0f) : 0.0f;
-                want = kl;
-                if (MODE == CB_PRE)
-                    grp = kl ? ld_nc_s32(crow + row * k + lane) : 0;
-            }
+            slot = kl ? ld_nc_s32(slot_of + row * k + lane) : 0;
+            // a null weight array means unit weights (the gradient of dispatch)
+            w = kl ? (topk_w ? ld_nc_f32(topk_w + row * k + lane) : 1.0f) : 0.0f;
+            want = kl;
+            grp = MODE == CB_COAL && kl ? ld_nc_s32(crow + row * k + lane) : 0;
         };
         int32_t cur_slot, nxt_slot = 0, cur_grp, nxt_grp = 0;
         float cur_w, nxt_w = 0.0f;
@@ -279,11 +291,11 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
             }
             const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
             const bool ok = cur_want && (unsigned)cur_slot < (unsigned)bound &&
-                            (MODE != CB_PRE || (unsigned)cur_grp < (unsigned)gbound);
+                            (MODE != CB_COAL || (unsigned)cur_grp < (unsigned)gbound);
             const unsigned okmask = __ballot_sync(FULL_MASK, ok);
             const unsigned wantmask = __ballot_sync(FULL_MASK, cur_want);
             float *h = hdr + s * CT_HDR_WORDS;
-            if (MODE == CB_PRE) {
+            if (MODE == CB_COAL) {
                 // groups of valid slots sharing a coalesced row, led by their first slot
                 const unsigned same = __match_any_sync(FULL_MASK, ok ? cur_grp : -1) & okmask;
                 const bool lead = ok && (same & lanemask_lt()) == 0;
@@ -348,12 +360,17 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         const int cb = (int)min((int64_t)CH, rowbytes - (int64_t)c * CH);
         const uint32_t base = stages + (uint32_t)s * stage_bytes;
         const int64_t out_elem0 = t * H + (int64_t)c * (CH / 2);
-        if (MODE == CB_PRE) {
-            // one output row per group; members in increasing slot order
+        if (MODE == CB_COAL) {
+            // one partial row per group (members in increasing slot order),
+            // and the token's sum of the rounded rows in group order
             const uint32_t *hu = reinterpret_cast<const uint32_t *>(h);
             const unsigned leaders = hu[CT_HDR_LEAD];
             const int64_t col0 = (int64_t)c * (CH / 2);
             for (int v = lane; v < cb / 16; v += 32) {
+                float tot[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    tot[i] = 0.0f;
                 for (unsigned ls = leaders; ls; ls &= ls - 1) {
                     const int o = __ffs(ls) - 1;
                     float acc[8];
@@ -378,8 +395,14 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                         rr[hh] = *reinterpret_cast<const uint32_t *>(&b);
                     }
                     const int64_t e0 = (int64_t)(int32_t)hu[CT_HDR_ROW + o] * H + col0 + (int64_t)v * 8;
-                    st_v4(static_cast<__nv_bfloat16 *>(out) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
+                    st_v4(static_cast<__nv_bfloat16 *>(part) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        tot[2 * hh] = __fadd_rn(tot[2 * hh], bf16lo(rr[hh]));
+                        tot[2 * hh + 1] = __fadd_rn(tot[2 * hh + 1], bf16hi(rr[hh]));
+                    }
                 }
+                store_row8(out, out_f32, out_elem0 + (int64_t)v * 8, tot);
             }
         } else {
             for (int v = lane; v < cb / 16; v += 32) {
@@ -399,22 +422,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                         }
                     }
                 }
-                const int64_t e0 = out_elem0 + (int64_t)v * 8;
-                if (out_f32) {
-                    float *o = static_cast<float *>(out) + e0;
-                    st_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                                        __float_as_uint(acc[2]), __float_as_uint(acc[3])));
-                    st_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
-                                            __float_as_uint(acc[6]), __float_as_uint(acc[7])));
-                } else {
-                    uint32_t rr[4];
-#pragma unroll
-                    for (int hh = 0; hh < 4; ++hh) {
-                        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * hh], acc[2 * hh + 1]);
-                        rr[hh] = *reinterpret_cast<const uint32_t *>(&b);
-                    }
-                    st_v4(static_cast<__nv_bfloat16 *>(out) + e0, make_uint4(rr[0], rr[1], rr[2], rr[3]));
-                }
+                store_row8(out, out_f32, out_elem0 + (int64_t)v * 8, acc);
             }
         }
         __syncwarp();
@@ -428,13 +436,14 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
 #endif
 }
 
-// T tokens; slot indices must lie in [0, bound) and (CB_PRE) output rows in
+// T tokens; slot indices must lie in [0, bound) and (CB_COAL) partial rows in
 // [0, gbound).
 template <int KMAX, int MODE>
 static cudaError_t launch_combine_bulk(int T, int H, int k, const void *y,
                                        const int32_t *slot_of, const float *topk_w,
-                                       const int32_t *crow, void *out, bool out_f32, int bound,
-                                       int gbound, uint32_t *err_word, cudaStream_t stream)
+                                       const int32_t *crow, void *part, void *out, bool out_f32,
+                                       int bound, int gbound, uint32_t *err_word,
+                                       cudaStream_t stream)
 {
     // Equal chunks (multiples of 16 bytes) of about CT_STAGE_TARGET / k bytes:
     // the fewest chunks per row whose k-row stage fits the target.
@@ -462,7 +471,7 @@ static cudaError_t launch_combine_bulk(int T, int H, int k, const void *y,
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const int64_t g = units < cap ? units : cap;
     return launch_pdl(kern, dim3((unsigned)g), dim3(CT_THREADS), smem, stream,
-                      static_cast<const uint8_t *>(y), slot_of, topk_w, crow, out,
+                      static_cast<const uint8_t *>(y), slot_of, topk_w, crow, part, out,
                       out_f32 ? 1 : 0, T, H, k, bound, gbound, CH, nchunks, units, err_word);
 }
 
@@ -790,17 +799,17 @@ cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *sl
         return cudaSuccess;
     const int N = T * k;
     if (k <= 8)
-        return launch_combine_bulk<8, CB_PLAIN>(T, H, k, y, slot_of, topk_w, nullptr, out,
-                                                out_f32, N, 0, err_word, stream);
+        return launch_combine_bulk<8, CB_PLAIN>(T, H, k, y, slot_of, topk_w, nullptr, nullptr,
+                                                out, out_f32, N, 0, err_word, stream);
     if (k <= 32)
-        return launch_combine_bulk<32, CB_PLAIN>(T, H, k, y, slot_of, topk_w, nullptr, out,
-                                                 out_f32, N, 0, err_word, stream);
+        return launch_combine_bulk<32, CB_PLAIN>(T, H, k, y, slot_of, topk_w, nullptr, nullptr,
+                                                 out, out_f32, N, 0, err_word, stream);
     // KC x U ~ 16 independent 16-byte loads in flight per lane.
     return launch_combine_t<8, 2>(T, H, k, y, slot_of, topk_w, out, out_f32, err_word, stream);
 }
 
-// Coalesced combine: the rank-side pre-reduction into `partial` (one bf16 row
-// per coalesced row), then the token-side sum of each token's distinct rows.
+// Coalesced combine, one pass: the rank-side pre-reduction into `partial` (one
+// bf16 row per coalesced row) and the token-side sum of the rounded rows.
 template <int KMAX>
 static cudaError_t launch_combine_coalesced_t(int T, int H, int k, const void *y,
                                               const int32_t *slot_of, const float *topk_w,
@@ -808,12 +817,8 @@ static cudaError_t launch_combine_coalesced_t(int T, int H, int k, const void *y
                                               void *out, bool out_f32, uint32_t *err_word,
                                               cudaStream_t stream)
 {
-    cudaError_t e = launch_combine_bulk<KMAX, CB_PRE>(T, H, k, y, slot_of, topk_w, crow, partial,
-                                                      false, T * k, rows, err_word, stream);
-    if (e != cudaSuccess)
-        return e;
-    return launch_combine_bulk<KMAX, CB_POST>(T, H, k, partial, nullptr, nullptr, crow, out,
-                                              out_f32, rows, 0, err_word, stream);
+    return launch_combine_bulk<KMAX, CB_COAL>(T, H, k, y, slot_of, topk_w, crow, partial, out,
+                                              out_f32, T * k, rows, err_word, stream);
 }
 
 cudaError_t launch_combine_coalesced(int T, int H, int k, const void *y, const int32_t *slot_of,

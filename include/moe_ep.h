@@ -290,7 +290,8 @@ MOE_API moe_status moe_dispatch_coalesced(int T, int H, int k, const void *x,
  *            sum from +0 of the token's distinct rows, in order of their
  *            first slot, rounded once
  *
- * Two launches, both token-major.  1 <= k <= 32 (larger k:
+ * One token-major launch (each unit folds a token's slots into its rows and
+ * sums them for the token in the same pass).  1 <= k <= 32 (larger k:
  * MOE_ERR_UNSUPPORTED); H % 8 == 0.  Rows of crow outside [0, rows) set
  * MOE_ERRBIT_BAD_INDEX and are skipped.  Not bit-identical to moe_combine:
  * each rank's share is rounded to bf16.
