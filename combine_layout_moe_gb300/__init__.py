@@ -33,6 +33,8 @@ SIGNATURES = {
     "moe_layout_workspace_bytes": ([_I, _I, _I], ctypes.c_size_t),
     "moe_layout": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P], ctypes.c_int),
     "moe_dispatch": ([_I, _I, _I, _P, _P, _P, _U32P, _P], ctypes.c_int),
+    "moe_layout_dispatch": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P,
+                             _P], ctypes.c_int),
     "moe_dispatch_quant": ([_I, _I, _I, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_combine": ([_I, _I, _I, _P, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_read_error": ([_U32P, _I, _P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
@@ -255,6 +257,39 @@ def moe_combine_coalesced(y: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.
     return out, partial
 
 
+def moe_layout_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, E: int, R: int, *,
+                        workspace: Optional[torch.Tensor] = None,
+                        out: Optional[Layout] = None, recv: Optional[torch.Tensor] = None,
+                        err_word: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None):
+    """moe_layout then moe_dispatch (bf16), the dispatch's first loads of x
+    overlapping the layout.  Returns (Layout, recv)."""
+    if topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be [T, k]")
+    T, k = topk_idx.shape
+    H = x.shape[1]
+    _want(topk_idx, "topk_idx", torch.int32)
+    _want(x, "x", torch.bfloat16, (T, H))
+    dev = topk_idx.device
+    if out is None:
+        out = Layout(torch.empty(E, dtype=torch.int32, device=dev),
+                     torch.empty(E + 1, dtype=torch.int32, device=dev),
+                     torch.empty(R + 1, dtype=torch.int32, device=dev),
+                     torch.empty((T, k), dtype=torch.int32, device=dev),
+                     torch.empty(T * k, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = new_workspace(moe_layout_workspace_bytes(T, k, E), dev)
+    if recv is None:
+        recv = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+    _check(_lib.moe_layout_dispatch(T, H, k, E, R, _ptr(topk_idx), _ptr(x),
+                                    _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                    _ptr(out.rank_offsets), _ptr(out.slot_of), _ptr(out.src_of),
+                                    _ptr(recv), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _ptr(err_word), _stream(stream)), "moe_layout_dispatch")
+    return out, recv
+
+
 def moe_dispatch(x: torch.Tensor, slot_of: torch.Tensor, *, recv: Optional[torch.Tensor] = None,
                  err_word: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
@@ -439,6 +474,7 @@ def moe_read_error(err_word: torch.Tensor, clear: bool = True,
 __all__ = [
     "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word", "new_workspace",
     "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
+    "moe_layout_dispatch",
     "moe_combine", "moe_read_error", "moe_sync_words", "SyncState",
     "moe_combine_backward", "moe_dispatch_backward",
     "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_combine_coalesced",

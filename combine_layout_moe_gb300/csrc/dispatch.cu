@@ -46,11 +46,17 @@ static_assert(DB_STAGES >= 2 && DB_STAGES <= 16, "stage ring size");
 // destination rank).  slot_of is then the coalesced row map, where every slot
 // of a token on one rank names the same row; only the lowest such slot
 // stores it, so each row is written once.  `rows` bounds the row indices.
+//
+// prefetch_x: the first stages' loads of x are issued before waiting on the
+// previous grid.  Only for a launch whose previous grid is this library's
+// layout kernel: that kernel lets dependents launch only after its own wait,
+// so x (written before the layout) is final, and only slot_of is not.
 template <bool COAL>
 __global__ void __launch_bounds__(32)
     dispatch_bulk_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ slot_of,
                          uint8_t *__restrict__ recv, int T, int k, int64_t rowbytes, int CH,
-                         int nchunks, int64_t units, int rows, uint32_t *err_word)
+                         int nchunks, int64_t units, int rows, int prefetch_x,
+                         uint32_t *err_word)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t bars = smem_addr(smem);
@@ -64,14 +70,10 @@ __global__ void __launch_bounds__(32)
         mbar_fence_init();
     }
     __syncwarp();
-    wait_prior_grid();
-    allow_next_grid();
 
     const int64_t u0 = units * blockIdx.x / gridDim.x;
     const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
     const int64_t nloc = u1 - u0;
-    if (nloc <= 0)
-        return;
 
     // load cursor (lane 0 issues loads in unit order)
     int64_t lt = u0 / nchunks;
@@ -90,6 +92,14 @@ __global__ void __launch_bounds__(32)
             ++lt;
         }
     };
+    if (prefetch_x) {
+        while (loaded < nloc && loaded < DB_STAGES)
+            issue_load();
+    }
+    wait_prior_grid();
+    allow_next_grid();
+    if (nloc <= 0)
+        return;
     while (loaded < nloc && loaded < DB_STAGES)
         issue_load();
 
@@ -307,7 +317,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
 template <bool COAL>
 static cudaError_t launch_dispatch_bulk(int T, int H, int k, const void *x,
                                        const int32_t *slot_of, void *recv, int rows,
-                                       uint32_t *err_word, cudaStream_t stream)
+                                       bool prefetch_x, uint32_t *err_word, cudaStream_t stream)
 {
     const int64_t rowbytes = 2 * (int64_t)H;
     const int CH = rowbytes < DB_CHUNK ? (int)rowbytes : DB_CHUNK;
@@ -329,7 +339,7 @@ static cudaError_t launch_dispatch_bulk(int T, int H, int k, const void *x,
     const int64_t g = units < cap ? units : cap;
     return launch_pdl(dispatch_bulk_kernel<COAL>, dim3((unsigned)g), dim3(32), smem, stream,
                       static_cast<const uint8_t *>(x), slot_of, static_cast<uint8_t *>(recv), T, k,
-                      rowbytes, CH, nchunks, units, rows, err_word);
+                      rowbytes, CH, nchunks, units, rows, prefetch_x ? 1 : 0, err_word);
 }
 
 cudaError_t launch_dispatch_coalesced(int T, int H, int k, const void *x, const int32_t *crow,
@@ -338,7 +348,7 @@ cudaError_t launch_dispatch_coalesced(int T, int H, int k, const void *x, const 
 {
     if (T == 0)
         return cudaSuccess;
-    return launch_dispatch_bulk<true>(T, H, k, x, crow, recv_c, rows, err_word, stream);
+    return launch_dispatch_bulk<true>(T, H, k, x, crow, recv_c, rows, false, err_word, stream);
 }
 
 cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32_t *slot_of,
@@ -347,7 +357,8 @@ cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32
     if (T == 0)
         return cudaSuccess;
     if (k <= 32)
-        return launch_dispatch_bulk<false>(T, H, k, x, slot_of, recv, T * k, err_word, stream);
+        return launch_dispatch_bulk<false>(T, H, k, x, slot_of, recv, T * k, false, err_word,
+                                           stream);
     const int C = H / 8;
     const int groups = (C + 32 * DISPATCH_U - 1) / (32 * DISPATCH_U);
     const int64_t items = (int64_t)T * groups;
@@ -356,6 +367,22 @@ cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32
     return launch_pdl(dispatch_bf16_kernel<DISPATCH_U>, dim3(grid), dim3(DISPATCH_THREADS), 0,
                       stream, static_cast<const uint4 *>(x), slot_of, static_cast<uint4 *>(recv),
                       k, C, groups, items, T * k, err_word);
+}
+
+cudaError_t launch_layout_dispatch(int T, int H, int k, int E, int R, const int32_t *topk_idx,
+                                   const void *x, int32_t *expert_counts,
+                                   int32_t *expert_offsets, int32_t *rank_offsets,
+                                   int32_t *slot_of, int32_t *src_of, void *recv,
+                                   void *workspace, uint32_t *err_word, cudaStream_t stream)
+{
+    cudaError_t e = launch_layout(T, k, E, R, topk_idx, expert_counts, expert_offsets,
+                                  rank_offsets, slot_of, src_of, workspace, err_word, stream);
+    if (e != cudaSuccess || T == 0)
+        return e;
+    if (k <= 32)  // the layout kernel is the previous grid: x may be read early
+        return launch_dispatch_bulk<false>(T, H, k, x, slot_of, recv, T * k, true, err_word,
+                                           stream);
+    return launch_dispatch_bf16(T, H, k, x, slot_of, recv, err_word, stream);
 }
 
 cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,

@@ -28,6 +28,14 @@ cudaError_t launch_dispatch_coalesced(int T, int H, int k, const void *x, const 
 cudaError_t launch_dispatch_bf16(int T, int H, int k, const void *x, const int32_t *slot_of,
                                  void *recv, uint32_t *err_word, cudaStream_t stream);
 
+// moe_layout followed by moe_dispatch (bf16) whose first loads of x overlap
+// the layout.
+cudaError_t launch_layout_dispatch(int T, int H, int k, int E, int R, const int32_t *topk_idx,
+                                   const void *x, int32_t *expert_counts,
+                                   int32_t *expert_offsets, int32_t *rank_offsets,
+                                   int32_t *slot_of, int32_t *src_of, void *recv,
+                                   void *workspace, uint32_t *err_word, cudaStream_t stream);
+
 cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
                                 uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
                                 cudaStream_t stream);

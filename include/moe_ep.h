@@ -136,6 +136,23 @@ MOE_API moe_status moe_dispatch(int T, int H, int k, const void *x, const int32_
                         void *recv, uint32_t *err_word, cudaStream_t stream);
 
 /*
+ * moe_layout_dispatch -- moe_layout followed by moe_dispatch (bf16), with the
+ * dispatch's first loads of x overlapping the layout.
+ *
+ * UBEP, section 3.2 (kernel decomposition: token sending overlaps the count
+ * and scan instead of waiting behind them).  Same arguments, outputs, rules
+ * and errors as moe_layout and moe_dispatch called in turn on `stream`.  The
+ * dispatch kernel may read x while the layout kernel still runs, which is
+ * safe here because x must be complete before this call, as for moe_dispatch.
+ */
+MOE_API moe_status moe_layout_dispatch(int T, int H, int k, int E, int R,
+                               const int32_t *topk_idx, const void *x,
+                               int32_t *expert_counts, int32_t *expert_offsets,
+                               int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
+                               void *recv, void *workspace, size_t workspace_bytes,
+                               uint32_t *err_word, cudaStream_t stream);
+
+/*
  * moe_dispatch_quant -- dispatch with fused FP8-E4M3 block quantisation.
  *
  * UBEP, Table 3 (the DeepSeek-R1 / V3.2 deployments run W8A8; the pages give no

@@ -320,3 +320,32 @@ def test_combine_bad_slot_reported():
     w = torch.ones((4, 2), dtype=torch.float32, device="cuda")
     m.moe_combine(y, so, w, err_word=err)
     assert m.moe_read_error(err) == m.MOE_ERRBIT_BAD_INDEX
+
+
+# ------------------------------------------------------- layout + dispatch
+
+@pytest.mark.parametrize("name", CONFIG_ORDER)
+def test_layout_dispatch_matches_oracle(name):
+    """The combined call, whose dispatch reads x while the layout still runs,
+    gives the layout and rows of the two calls made in turn."""
+    m = cl()
+    w = workload(name)
+    lay, recv = m.moe_layout_dispatch(bf16_dev(w.x), i32_dev(w.topk_idx), w.E, w.R)
+    torch.cuda.synchronize()
+    o = oracle.layout(w.topk_idx, w.E, w.R)
+    for a, b in zip(lay, o):
+        assert np.array_equal(a.cpu().numpy(), b)
+    assert np.array_equal(bits(recv), oracle.dispatch(w.x, o[3]))
+
+
+@pytest.mark.parametrize("case", [(71, 1, 8, 1, 1, 1), (72, 300, 1000, 33, 64, 8),
+                                  (73, 5000, 2048, 8, 256, 32), (74, 0, 64, 2, 4, 2)])
+def test_layout_dispatch_fuzz(case):
+    m = cl()
+    seed, T, H, k, E, R = case
+    w = random_case(seed, T, H, k, E, R)
+    lay, recv = m.moe_layout_dispatch(bf16_dev(w.x), i32_dev(w.topk_idx), E, R)
+    torch.cuda.synchronize()
+    o = oracle.layout(w.topk_idx, E, R)
+    assert np.array_equal(lay.slot_of.cpu().numpy(), o[3])
+    assert np.array_equal(bits(recv), oracle.dispatch(w.x, o[3]))
