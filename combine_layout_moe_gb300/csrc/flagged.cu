@@ -9,7 +9,10 @@
 //
 // Structure: one cooperative launch, every warp resident.  Each warp runs
 // three phases over its own contiguous range of units; a unit is W bytes of
-// one row, W = max(G, 512), where G is the synchronisation granularity:
+// one row -- W = max(G, 2048), or one batch (BATCH) -- where G is the
+// synchronisation granularity.  A lane issues the loads of four 512-byte warp
+// steps before it stores any of them, and combine loads up to eight slots'
+// rows before folding them:
 //   produce  (token t, unit): x[t] -> the k rows slot_of[t, :] of recv
 //   expert   (receive row s, unit), in receive (expert-major) order:
 //            recv[s] -> y[s] (the identity expert)
@@ -54,6 +57,16 @@ namespace moe {
 constexpr int DF_THREADS = 256;
 constexpr int DF_WARPS = DF_THREADS / 32;
 constexpr int DF_STEP = 512;  // bytes a warp moves per step: 32 lanes x 16 B
+// Tunables (compile-time; the defaults are the shipped configuration).
+#ifndef MOE_DF_ILP
+#define MOE_DF_ILP 4
+#endif
+#ifndef MOE_DF_MINB
+#define MOE_DF_MINB 4
+#endif
+constexpr int DF_ILP = MOE_DF_ILP;  // steps whose loads a lane issues before storing
+constexpr int DF_JG = 8;      // slots whose rows combine loads before folding
+constexpr int DF_UNIT = DF_STEP * DF_ILP;  // smallest unit (WORD, SENTINEL, BARRIER)
 constexpr uint32_t DF_SENTINEL = 0xFFFFFFFFu;
 
 __device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v)
@@ -142,7 +155,7 @@ struct DfArgs {
     int out_f32;
     int T, k, C;  // tokens, slots per token, 16-byte vectors per row
     int G;        // synchronisation granularity in bytes
-    int W;        // unit bytes, max(G, DF_STEP)
+    int W;        // unit bytes: G (BATCH) or max(G, DF_UNIT)
     int upr;      // units per row
     int nblk;     // G-byte blocks per row
     uint32_t *words;
@@ -153,7 +166,7 @@ struct DfArgs {
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(const DfArgs a)
+__global__ void __launch_bounds__(DF_THREADS, MOE_DF_MINB) dispatch_combine_flagged_kernel(const DfArgs a)
 {
     wait_prior_grid();
     allow_next_grid();
@@ -174,9 +187,33 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
             report(a.err, MOE_ERRBIT_TIMEOUT);
         give_up = true;
     };
-    // the G-block of this lane's vector in unit cu (G < 512: one step per
-    // unit; G >= 512: the unit is one block)
-    auto lane_block = [&](int cu) { return (cu * a.W + (a.G < DF_STEP ? lane * 16 : 0)) / a.G; };
+    // vector of this lane in step q of unit cu
+    auto vec = [&](int cu, int q) { return cu * vpu + q * 32 + lane; };
+    // WORD: wait (this lane alone) for the word of every block its vectors of
+    // unit cu of row s fall in; false if a wait ran out
+    auto wait_blocks = [&](const uint32_t *words, int64_t s, int cu, uint64_t limit) {
+        bool ok = true;
+        int last = -1;
+        for (int q = 0; q < nsteps; ++q) {
+            const int v = vec(cu, q);
+            if (v >= C)
+                break;
+            const int b = v * 16 / a.G;
+            if (b == last)
+                continue;
+            last = b;
+            const uint32_t *w = words + (size_t)s * a.nblk + b;
+            ok = ok && spin_until([&] { return ld_acquire_u32(w) == a.epoch; }, limit,
+                                  give_up || !ok);
+        }
+        return ok;
+    };
+    // WORD: publish the words of the blocks of unit cu of row s (after a fence)
+    auto publish_blocks = [&](uint32_t *words, int64_t s, int cu) {
+        const int b0 = cu * a.W / a.G, nb = a.W / a.G;
+        for (int b = lane; b < nb && b0 + b < a.nblk; b += 32)
+            st_relaxed_u32(words + (size_t)s * a.nblk + b0 + b, a.epoch);
+    };
 
     // ------------------------------------------------------------ produce
     {
@@ -185,28 +222,37 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
             const int64_t t = u / a.upr;
             const int cu = (int)(u - t * a.upr);
             const int32_t mine = lane < k ? ld_nc_s32(a.slot_of + t * k + lane) : -1;
-            uint32_t csum = 0;
+            uint32_t csum = 0;  // lane 0: the first word of each 512-byte block
             bool hit = false;
-            for (int q = 0; q < nsteps; ++q) {
-                const int v = cu * vpu + q * 32 + lane;
-                const bool in = v < C;
-                const uint4 d = in ? ld_stream_v4(a.x + t * C + v) : make_uint4(0, 0, 0, 0);
-                csum += d.x;  // lane 0: the first word of each 512-byte block
-                hit |= in && has_sentinel(d);
+            for (int q0 = 0; q0 < nsteps; q0 += DF_ILP) {
+                uint4 d[DF_ILP];
+                bool in[DF_ILP];
+#pragma unroll
+                for (int r = 0; r < DF_ILP; ++r) {
+                    const int v = vec(cu, q0 + r);
+                    in[r] = q0 + r < nsteps && v < C;
+                    d[r] = in[r] ? ld_stream_v4(a.x + t * C + v) : make_uint4(0, 0, 0, 0);
+                    csum += d[r].x;
+                    hit |= in[r] && has_sentinel(d[r]);
+                }
                 for (int j = 0; j < k; ++j) {
                     const int32_t s = __shfl_sync(FULL_MASK, mine, j);
                     if ((unsigned)s >= (unsigned)N) {
-                        if (lane == 0 && cu == 0 && q == 0)
+                        if (lane == 0 && cu == 0 && q0 == 0)
                             report(a.err, MOE_ERRBIT_BAD_INDEX);
                         continue;
                     }
-                    if (!in)
+                    if (MODE == MOE_SYNC_SENTINEL && t * k + j == a.skip_pair)
                         continue;
-                    if (MODE == MOE_SYNC_SENTINEL) {
-                        if (t * k + j != a.skip_pair)
-                            st_volatile_v4(a.recv + (int64_t)s * C + v, d);
-                    } else {
-                        st_v4(a.recv + (int64_t)s * C + v, d);
+#pragma unroll
+                    for (int r = 0; r < DF_ILP; ++r) {
+                        if (!in[r])
+                            continue;
+                        uint4 *dst = a.recv + (int64_t)s * C + vec(cu, q0 + r);
+                        if (MODE == MOE_SYNC_SENTINEL)
+                            st_volatile_v4(dst, d[r]);
+                        else
+                            st_v4(dst, d[r]);
                     }
                 }
             }
@@ -216,24 +262,18 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
                 continue;
             __threadfence();  // this lane's row stores, before any word below
             __syncwarp();
-            if (MODE == MOE_SYNC_WORD) {
-                // one word per (slot row, block of this unit)
-                const int b0 = cu * a.W / a.G;
-                const int nb = a.G < DF_STEP ? DF_STEP / a.G : 1;
-                for (int base = 0; base < k * nb; base += 32) {
-                    const int f = base + lane;
-                    const int j = f < k * nb ? f / nb : 0;
-                    const int32_t s = __shfl_sync(FULL_MASK, mine, j);
-                    const int b = b0 + f % nb;
-                    if (f < k * nb && b < a.nblk && (unsigned)s < (unsigned)N &&
-                        t * k + j != a.skip_pair)
-                        st_relaxed_u32(dwords + (size_t)s * a.nblk + b, a.epoch);
+            for (int j = 0; j < k; ++j) {
+                const int32_t s = __shfl_sync(FULL_MASK, mine, j);
+                if ((unsigned)s >= (unsigned)N || t * k + j == a.skip_pair)
+                    continue;
+                if (MODE == MOE_SYNC_WORD) {
+                    publish_blocks(dwords, s, cu);
+                } else {
+                    const uint32_t sum = __shfl_sync(FULL_MASK, csum, 0);
+                    if (lane == 0)
+                        st_relaxed_u64(dbatch + (size_t)s * a.nblk + cu,
+                                       ((unsigned long long)a.epoch << 32) | sum);
                 }
-            } else {
-                const uint32_t sum = __shfl_sync(FULL_MASK, csum, 0);
-                if (lane < k && (unsigned)mine < (unsigned)N && t * k + lane != a.skip_pair)
-                    st_relaxed_u64(dbatch + (size_t)mine * a.nblk + cu,
-                                   ((unsigned long long)a.epoch << 32) | sum);
             }
         }
     }
@@ -247,13 +287,8 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
         for (int64_t u = u0; u < u1; ++u) {
             const int64_t s = u / a.upr;
             const int cu = (int)(u - s * a.upr);
-            const bool lane_has = cu * vpu + lane < C;  // this lane has a vector in the unit
             if (MODE == MOE_SYNC_WORD) {
-                const uint32_t *w = dwords + (size_t)s * a.nblk + lane_block(cu);
-                const bool r =
-                    !lane_has ||
-                    spin_until([&] { return ld_acquire_u32(w) == a.epoch; }, a.spin_ns, give_up);
-                if (!__all_sync(FULL_MASK, r)) {
+                if (!__all_sync(FULL_MASK, wait_blocks(dwords, s, cu, a.spin_ns))) {
                     timed_out();
                     continue;
                 }
@@ -269,30 +304,41 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
             }
             uint32_t csum = 0;
             bool ok = true;
-            for (int q = 0; q < nsteps; ++q) {
-                const int v = cu * vpu + q * 32 + lane;
-                if (v >= C)
-                    continue;
-                uint4 *src = a.recv + s * C + v;
-                uint4 d;
-                if (MODE == MOE_SYNC_SENTINEL) {
-                    const bool r = spin_until(
-                        [&] {
-                            d = ld_volatile_v4(src);
-                            return !has_sentinel(d);
-                        },
-                        a.spin_ns, give_up || !ok);
-                    if (!r) {
-                        ok = false;
-                        continue;
-                    }
-                    st_volatile_v4(a.y + s * C + v, d);
-                    st_volatile_v4(src, sentinel4());
-                } else {
-                    d = ld_cg_v4(src);
-                    st_v4(a.y + s * C + v, d);
+            for (int q0 = 0; q0 < nsteps; q0 += DF_ILP) {
+                uint4 d[DF_ILP];
+                bool in[DF_ILP];
+#pragma unroll
+                for (int r = 0; r < DF_ILP; ++r) {
+                    const int v = vec(cu, q0 + r);
+                    in[r] = q0 + r < nsteps && v < C;
+                    d[r] = make_uint4(0, 0, 0, 0);
+                    if (in[r])
+                        d[r] = MODE == MOE_SYNC_SENTINEL ? ld_volatile_v4(a.recv + s * C + v)
+                                                         : ld_cg_v4(a.recv + s * C + v);
                 }
-                csum += d.x;
+#pragma unroll
+                for (int r = 0; r < DF_ILP; ++r) {
+                    if (!in[r])
+                        continue;
+                    uint4 *src = a.recv + s * C + vec(cu, q0 + r);
+                    if (MODE == MOE_SYNC_SENTINEL) {
+                        if (has_sentinel(d[r]) &&
+                            !spin_until(
+                                [&] {
+                                    d[r] = ld_volatile_v4(src);
+                                    return !has_sentinel(d[r]);
+                                },
+                                a.spin_ns, give_up || !ok)) {
+                            ok = false;
+                            continue;
+                        }
+                        st_volatile_v4(a.y + s * C + vec(cu, q0 + r), d[r]);
+                        st_volatile_v4(src, sentinel4());
+                    } else {
+                        st_v4(a.y + s * C + vec(cu, q0 + r), d[r]);
+                    }
+                    csum += d[r].x;
+                }
             }
             if (MODE == MOE_SYNC_SENTINEL) {
                 if (!__all_sync(FULL_MASK, ok))
@@ -307,10 +353,7 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
             __threadfence();
             __syncwarp();
             if (MODE == MOE_SYNC_WORD) {
-                const int b0 = cu * a.W / a.G;
-                const int nb = a.G < DF_STEP ? DF_STEP / a.G : 1;
-                if (lane < nb && b0 + lane < a.nblk)
-                    st_relaxed_u32(ewords + (size_t)s * a.nblk + b0 + lane, a.epoch);
+                publish_blocks(ewords, s, cu);
             } else if (lane == 0) {
                 st_relaxed_u64(ebatch + (size_t)s * a.nblk + cu,
                                ((unsigned long long)a.epoch << 32) | csum);
@@ -332,7 +375,6 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
             const int cu = (int)(u - t * a.upr);
             const int32_t ms = lane < k ? ld_nc_s32(a.slot_of + t * k + lane) : 0;
             const float mw = lane < k ? ld_nc_f32(a.topk_w + t * k + lane) : 0.0f;
-            const bool lane_has = cu * vpu + lane < C;
             bool ok = true;
             if (MODE == MOE_SYNC_WORD || MODE == MOE_SYNC_BATCH) {
                 for (int j = 0; j < k && ok; ++j) {
@@ -341,9 +383,7 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
                         continue;
                     bool r;
                     if (MODE == MOE_SYNC_WORD) {
-                        const uint32_t *w = ewords + (size_t)s * a.nblk + lane_block(cu);
-                        r = !lane_has || spin_until([&] { return ld_acquire_u32(w) == a.epoch; },
-                                                    climit, give_up);
+                        r = wait_blocks(ewords, s, cu, climit);
                     } else {
                         const unsigned long long *w = ebatch + (size_t)s * a.nblk + cu;
                         r = spin_until(
@@ -359,45 +399,54 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
             }
             uint32_t csum = 0;  // lane j: the block markers of row j (BATCH)
             for (int q = 0; q < nsteps; ++q) {
-                const int v = cu * vpu + q * 32 + lane;
+                const int v = vec(cu, q);
                 const bool in = v < C;
                 float acc[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     acc[i] = 0.0f;
-                for (int j = 0; j < k; ++j) {
-                    const int32_t s = __shfl_sync(FULL_MASK, ms, j);
-                    const float w = __shfl_sync(FULL_MASK, mw, j);
-                    if ((unsigned)s >= (unsigned)N)
-                        continue;
-                    uint4 d = make_uint4(0, 0, 0, 0);
-                    if (in) {
-                        uint4 *src = a.y + (int64_t)s * C + v;
-                        if (MODE == MOE_SYNC_SENTINEL) {
-                            const bool r = spin_until(
-                                [&] {
-                                    d = ld_volatile_v4(src);
-                                    return !has_sentinel(d);
-                                },
-                                climit, give_up || !ok);
-                            if (r)
-                                st_volatile_v4(src, sentinel4());
-                            else
-                                ok = false;
-                        } else {
-                            d = ld_cg_v4(src);
-                        }
-                    }
-                    if (MODE == MOE_SYNC_BATCH) {
-                        const uint32_t marker = __shfl_sync(FULL_MASK, d.x, 0);
-                        if (lane == j)
-                            csum += marker;
-                    }
-                    const uint32_t p[4] = {d.x, d.y, d.z, d.w};
+                for (int jb = 0; jb < k; jb += DF_JG) {
+                    // the rows of up to DF_JG slots are loaded before any is used
+                    uint4 d[DF_JG];
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        acc[2 * h] = __fmaf_rn(w, bf16lo(p[h]), acc[2 * h]);
-                        acc[2 * h + 1] = __fmaf_rn(w, bf16hi(p[h]), acc[2 * h + 1]);
+                    for (int r = 0; r < DF_JG; ++r) {
+                        const int32_t s = __shfl_sync(FULL_MASK, ms, (jb + r) & 31);
+                        d[r] = make_uint4(0, 0, 0, 0);
+                        if (in && jb + r < k && (unsigned)s < (unsigned)N)
+                            d[r] = MODE == MOE_SYNC_SENTINEL ? ld_volatile_v4(a.y + (int64_t)s * C + v)
+                                                             : ld_cg_v4(a.y + (int64_t)s * C + v);
+                    }
+#pragma unroll
+                    for (int r = 0; r < DF_JG; ++r) {
+                        const int j = jb + r;
+                        const int32_t s = __shfl_sync(FULL_MASK, ms, j & 31);
+                        const float w = __shfl_sync(FULL_MASK, mw, j & 31);
+                        if (j >= k || (unsigned)s >= (unsigned)N)
+                            continue;
+                        if (MODE == MOE_SYNC_SENTINEL && in) {
+                            uint4 *src = a.y + (int64_t)s * C + v;
+                            if (has_sentinel(d[r]) &&
+                                !spin_until(
+                                    [&] {
+                                        d[r] = ld_volatile_v4(src);
+                                        return !has_sentinel(d[r]);
+                                    },
+                                    climit, give_up || !ok))
+                                ok = false;
+                            else
+                                st_volatile_v4(src, sentinel4());
+                        }
+                        if (MODE == MOE_SYNC_BATCH) {
+                            const uint32_t marker = __shfl_sync(FULL_MASK, d[r].x, 0);
+                            if (lane == j)
+                                csum += marker;
+                        }
+                        const uint32_t p[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            acc[2 * h] = __fmaf_rn(w, bf16lo(p[h]), acc[2 * h]);
+                            acc[2 * h + 1] = __fmaf_rn(w, bf16hi(p[h]), acc[2 * h + 1]);
+                        }
                     }
                 }
                 if (!in || !ok)
@@ -429,17 +478,22 @@ __global__ void __launch_bounds__(DF_THREADS) dispatch_combine_flagged_kernel(co
 }
 
 // Geometry of granularity G: unit bytes, units per row, blocks per row; false
-// when G is not a valid granularity for the mode.
+// when G is not a valid granularity for the mode.  A unit is one batch
+// (BATCH) or max(G, DF_UNIT) bytes, and holds whole blocks.
 static bool df_geometry(int mode, int H, int G, int &W, int &upr, int &nblk)
 {
     const int rowbytes = 2 * H;
     if (G < 16 || G % 16 != 0)
         return false;
-    if (G < DF_STEP ? DF_STEP % G != 0 : G % DF_STEP != 0)
-        return false;
-    if (mode == MOE_SYNC_BATCH && G % DF_STEP != 0)
-        return false;
-    W = G < DF_STEP ? DF_STEP : G;
+    if (mode == MOE_SYNC_BATCH) {
+        if (G % DF_STEP != 0)
+            return false;
+        W = G;
+    } else {
+        if (G < DF_UNIT ? DF_UNIT % G != 0 : G % DF_STEP != 0)
+            return false;
+        W = G < DF_UNIT ? DF_UNIT : G;
+    }
     upr = (rowbytes + W - 1) / W;
     nblk = (rowbytes + G - 1) / G;
     return true;

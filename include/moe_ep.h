@@ -335,8 +335,10 @@ MOE_API moe_status moe_combine_coalesced(int T, int H, int k, const void *y,
  * The expert and combine phases read rows written by other SMs; how they know
  * the rows have arrived is `mode`, at granularity `block_bytes` (G):
  *   MOE_SYNC_WORD      a 32-bit word per (row, G-byte block) per hop, set to
- *                      `epoch` after a fence; G in {16, 32, ..., 512} or a
- *                      multiple of 512
+ *                      `epoch` after a fence; G a power of two from 16 to
+ *                      1024, or a multiple of 512 from 2048 (a warp moves at
+ *                      least 2048 bytes of a row between fences, so blocks of
+ *                      one such unit are published together)
  *   MOE_SYNC_SENTINEL  no words.  recv and y must hold 0xFFFFFFFF in every
  *                      32-bit word before the call (memset 0xFF); readers
  *                      poll the data until no word is the sentinel and write
