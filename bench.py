@@ -17,10 +17,11 @@ rank runs its own replica).  `e2e` repeats the
 step through the public API with each step's inputs copied from pinned host
 memory and its combined output copied back, pipelined over three streams.
 
---variant coalesced times the rank-coalesced path instead (bf16 workloads):
-layout -> coalesced layout -> coalesced dispatch (one row per token and
-destination rank), then the coalesced combine (per-rank pre-reduction, then
-the per-token sum).  The default line is the plain path.
+--variant coalesced times the rank-coalesced path instead: layout ->
+coalesced layout -> coalesced dispatch (one row per token and destination
+rank; FP8 codes and scales for FP8 workloads), then the coalesced combine
+(per-rank pre-reduction and the per-token sum).  The default line is the plain
+path.
 
 --impl reference times the CPU oracle (the plain C statement of the method) on
 the same metric: every step is a bounded sample of the same workload recipe.
@@ -62,6 +63,7 @@ def kernel_bytes(name: str, T: int, H: int, k: int, E: int, R: int = 1) -> int:
     combine        reads k rows per token, slot_of and weights, writes one row
     The coalesced kernels also depend on Nc, the number of coalesced rows:
     dispatch_coalesced  reads x and crow, writes Nc rows
+    dispatch_fp8_coalesced  reads x and crow, writes Nc rows of codes and scales
     combine_coalesced   reads k rows per token, slot_of, weights and crow,
                         writes the Nc pre-reduced rows and one row per token
     """
@@ -83,6 +85,8 @@ def coalesced_bytes(name: str, T: int, H: int, k: int, Nc: int) -> int:
     N = T * k
     if name == "dispatch_coalesced":
         return 2 * T * H + 4 * N + 2 * Nc * H
+    if name == "dispatch_fp8_coalesced":
+        return 2 * T * H + 4 * N + Nc * H + 4 * Nc * (H // 128)
     if name == "combine_coalesced":
         return 2 * N * H + 12 * N + 2 * Nc * H + 2 * T * H
     raise KeyError(name)
@@ -310,7 +314,7 @@ def run_gpu(args):
     name = args.config
     c = CONFIGS[name]
     coal = args.variant == "coalesced"
-    fp8 = c["payload"] == "fp8" and not coal   # the coalesced variant moves bf16 rows
+    fp8 = c["payload"] == "fp8"
     w = make_workload(name, seed=args.seed + rank)
     T, H, k, E, R, N = w.T, w.H, w.k, w.E, w.R, w.N
 
@@ -327,11 +331,13 @@ def run_gpu(args):
                    torch.empty((T, k), dtype=torch.int32, device=dev),
                    torch.empty(T * k, dtype=torch.int32, device=dev))
     rows = T * min(k, R)   # coalesced rows: at most one per token and rank
+    nrecv = rows if coal else N
     if fp8:
-        recv_q = torch.empty((N, H), dtype=torch.uint8, device=dev)
-        recv_s = torch.empty((N, H // 128), dtype=torch.float32, device=dev)
-    elif coal:
-        recv = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        recv_q = torch.empty((nrecv, H), dtype=torch.uint8, device=dev)
+        recv_s = torch.empty((nrecv, H // 128), dtype=torch.float32, device=dev)
+    else:
+        recv = torch.empty((nrecv, H), dtype=torch.bfloat16, device=dev)
+    if coal:
         partial = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
         wsc = m.new_workspace(m.moe_layout_workspace_bytes(T, k, R), dev)
         co = m.CoalescedLayout(torch.empty(R, dtype=torch.int32, device=dev),
@@ -339,8 +345,6 @@ def run_gpu(args):
                                torch.empty((T, k), dtype=torch.int32, device=dev),
                                torch.empty(T * k, dtype=torch.int32, device=dev),
                                torch.empty(T * k, dtype=torch.int32, device=dev))
-    else:
-        recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -355,7 +359,10 @@ def run_gpu(args):
     P = lambda t: t.data_ptr()  # noqa: E731
     lay_args = (T, k, E, R, P(idx), P(lay.expert_counts), P(lay.expert_offsets),
                 P(lay.rank_offsets), P(lay.slot_of), P(lay.src_of), P(ws), ws.numel(), P(err), cs)
-    if fp8:
+    if fp8 and coal:
+        disp_fn, disp_args = L.moe_dispatch_quant_coalesced, (T, H, k, P(x), P(co.crow), rows,
+                                                              P(recv_q), P(recv_s), P(err), cs)
+    elif fp8:
         disp_fn, disp_args = L.moe_dispatch_quant, (T, H, k, P(x), P(lay.slot_of), P(recv_q),
                                                     P(recv_s), P(err), cs)
     elif coal:
@@ -482,7 +489,8 @@ def run_gpu(args):
 
     # roofline of the dominant kernel: combine is timed alone inside the timed
     # steps; dispatch (when it dominates) in the breakdown pass.
-    d_name = "dispatch_fp8" if fp8 else ("dispatch_coalesced" if coal else "dispatch_bf16")
+    d_name = (("dispatch_fp8_coalesced" if fp8 else "dispatch_coalesced") if coal
+              else ("dispatch_fp8" if fp8 else "dispatch_bf16"))
     c_name = "combine_coalesced" if coal else "combine"
     avg_d, avg_c = statistics.mean(t_disp), statistics.mean(t_comb)
     if avg_c >= avg_d:
@@ -495,6 +503,7 @@ def run_gpu(args):
     kern_name = {"dispatch_bf16": "dispatch_bulk_kernel", "dispatch_fp8": "dispatch_fp8_kernel",
                  "combine": "combine_bulk_kernel",
                  "dispatch_coalesced": "dispatch_bulk_kernel<coalesced>",
+                 "dispatch_fp8_coalesced": "dispatch_fp8_kernel<coalesced>",
                  "combine_coalesced": "combine_bulk_kernel<coalesced>"}[dom]
     tr = None if coal else recorded_traffic(kern_name)
     traffic = None
@@ -515,8 +524,8 @@ def run_gpu(args):
     ib = [idx, torch.empty_like(idx)]
     wb = [wt, torch.empty_like(wt)]
     ob = [out, torch.empty_like(out)]
-    rq = dict(recv_q=recv_q, recv_scales=recv_s) if fp8 else (dict(recv_c=recv) if coal
-                                                                else dict(recv=recv))
+    rq = (dict(recv_q=recv_q, recv_scales=recv_s) if fp8
+          else (dict(recv_c=recv) if coal else dict(recv=recv)))
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
     def e2e_run(n):
@@ -546,7 +555,12 @@ def run_gpu(args):
                 m.moe_layout(ib[b], E, R, workspace=ws, err_word=err, out=lay, stream=stream)
                 m.moe_layout_coalesced(ib[b], lay.slot_of, E, R, workspace=wsc, err_word=err,
                                        out=co, stream=stream)
-                m.moe_dispatch_coalesced(xb[b], co.crow, rows, err_word=err, stream=stream, **rq)
+                if fp8:
+                    m.moe_dispatch_quant_coalesced(xb[b], co.crow, rows, err_word=err,
+                                                   stream=stream, **rq)
+                else:
+                    m.moe_dispatch_coalesced(xb[b], co.crow, rows, err_word=err, stream=stream,
+                                             **rq)
                 m.moe_combine_coalesced(y, lay.slot_of, wb[b], co, rows, partial=partial,
                                         out=ob[b], err_word=err, stream=stream)
             else:
@@ -625,7 +639,7 @@ def main(argv=None):
                    help="tokens per oracle step in --impl reference")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--variant", choices=["plain", "coalesced"], default="plain",
-                   help="plain: the hot path; coalesced: the rank-coalesced path (bf16)")
+                   help="plain: the hot path; coalesced: the rank-coalesced path")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")

@@ -45,6 +45,7 @@ SIGNATURES = {
     "moe_layout_coalesced": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P],
                              ctypes.c_int),
     "moe_dispatch_coalesced": ([_I, _I, _I, _P, _P, _I, _P, _U32P, _P], ctypes.c_int),
+    "moe_dispatch_quant_coalesced": ([_I, _I, _I, _P, _P, _I, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_combine_coalesced": ([_I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _I, _U32P, _P],
                               ctypes.c_int),
     "moe_dispatch_combine_flagged": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P,
@@ -229,6 +230,29 @@ def moe_dispatch_coalesced(x: torch.Tensor, crow: torch.Tensor, rows: int, *,
     _check(_lib.moe_dispatch_coalesced(T, H, k, _ptr(x), _ptr(crow), rows, _ptr(recv_c),
                                        _ptr(err_word), _stream(stream)), "moe_dispatch_coalesced")
     return recv_c
+
+
+def moe_dispatch_quant_coalesced(x: torch.Tensor, crow: torch.Tensor, rows: int, *,
+                                 recv_q: Optional[torch.Tensor] = None,
+                                 recv_scales: Optional[torch.Tensor] = None,
+                                 err_word: Optional[torch.Tensor] = None,
+                                 stream: Optional[torch.cuda.Stream] = None):
+    """E4M3 codes and fp32 scales of each token, written once per coalesced
+    row.  Returns (recv_q uint8 [rows, H], recv_scales fp32 [rows, H/128])."""
+    T, H = x.shape
+    k = crow.shape[1]
+    _want(x, "x", torch.bfloat16)
+    _want(crow, "crow", torch.int32, (T, k))
+    if recv_q is None:
+        recv_q = torch.empty((rows, H), dtype=torch.uint8, device=x.device)
+    if recv_scales is None:
+        recv_scales = torch.empty((rows, H // 128), dtype=torch.float32, device=x.device)
+    if recv_q.shape[0] < rows or recv_scales.shape[0] < rows:
+        raise ValueError("recv_q / recv_scales have fewer than `rows` rows")
+    _check(_lib.moe_dispatch_quant_coalesced(T, H, k, _ptr(x), _ptr(crow), rows, _ptr(recv_q),
+                                             _ptr(recv_scales), _ptr(err_word), _stream(stream)),
+           "moe_dispatch_quant_coalesced")
+    return recv_q, recv_scales
 
 
 def moe_combine_coalesced(y: torch.Tensor, slot_of: torch.Tensor, topk_w: torch.Tensor,
@@ -477,6 +501,7 @@ __all__ = [
     "moe_layout_dispatch",
     "moe_combine", "moe_read_error", "moe_sync_words", "SyncState",
     "moe_combine_backward", "moe_dispatch_backward",
-    "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_combine_coalesced",
+    "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_dispatch_quant_coalesced",
+    "moe_combine_coalesced",
     "moe_dispatch_combine_flagged", "LIB_PATH", "SIGNATURES",
 ]

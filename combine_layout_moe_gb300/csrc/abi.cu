@@ -164,6 +164,23 @@ moe_status moe_dispatch_coalesced(int T, int H, int k, const void *x, const int3
                                                     stream));
 }
 
+moe_status moe_dispatch_quant_coalesced(int T, int H, int k, const void *x, const int32_t *crow,
+                                        int rows, uint8_t *recv_q, float *recv_scales,
+                                        uint32_t *err_word, cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || H < 128 || H % 128 != 0 || rows < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (k > 32)
+        return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !crow || !recv_q || !recv_scales))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv_q, 16) || !aligned(recv_scales, 16) ||
+        !aligned(crow, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_dispatch_fp8_coalesced(T, H, k, x, crow, recv_q, recv_scales,
+                                                        rows, err_word, stream));
+}
+
 moe_status moe_combine_coalesced(int T, int H, int k, const void *y, const int32_t *slot_of,
                                  const float *topk_w, const int32_t *crow, int rows,
                                  void *partial, void *out, int out_dtype, uint32_t *err_word,

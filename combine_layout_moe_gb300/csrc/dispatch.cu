@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
 // The amax is reduced with xor-shuffles inside the half-warp; scale and
 // reciprocal are each one correctly rounded fp32 division; each channel is one
 // rounded fp32 multiply followed by a saturating nearest-even E4M3 conversion.
-template <int U>
+template <int U, bool COAL>
 __global__ void __launch_bounds__(DISPATCH_THREADS)
     dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
                         uint8_t *__restrict__ recv_q, float *__restrict__ recv_scales, int k,
@@ -291,8 +291,17 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
         for (int jb = 0; jb < k; jb += 32) {
             const int32_t mine = jb + lane < k ? ld_nc_s32(so + jb + lane) : 0;
             const int jn = min(32, k - jb);
+            // COAL (k <= 32): a slot whose coalesced row a lower slot of the
+            // token names stores nothing; that row is written once
+            bool first = true;
+            if (COAL) {
+                const unsigned kmask = jn >= 32 ? FULL_MASK : (1u << jn) - 1u;
+                first = (__match_any_sync(FULL_MASK, mine) & kmask & lanemask_lt()) == 0;
+            }
             for (int q = 0; q < jn; ++q) {
                 const int32_t s = __shfl_sync(FULL_MASK, mine, q);
+                if (COAL && !__shfl_sync(FULL_MASK, first, q))
+                    continue;
                 if ((unsigned)s >= (unsigned)N) {
                     if (lane == 0)
                         report(err_word, MOE_ERRBIT_BAD_INDEX);
@@ -385,20 +394,36 @@ cudaError_t launch_layout_dispatch(int T, int H, int k, int E, int R, const int3
     return launch_dispatch_bf16(T, H, k, x, slot_of, recv, err_word, stream);
 }
 
-cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
-                                uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
-                                cudaStream_t stream)
+template <bool COAL>
+static cudaError_t launch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
+                              uint8_t *recv_q, float *recv_scales, int rows, uint32_t *err_word,
+                              cudaStream_t stream)
 {
     if (T == 0)
         return cudaSuccess;
     const int C = H / 8;
     const int groups = (C + 32 * QUANT_U - 1) / (32 * QUANT_U);
     const int64_t items = (int64_t)T * groups;
-    const int grid = warp_item_grid((const void *)dispatch_fp8_kernel<QUANT_U>,
-                                    DISPATCH_THREADS, 0, items);
-    return launch_pdl(dispatch_fp8_kernel<QUANT_U>, dim3(grid), dim3(DISPATCH_THREADS), 0,
-                      stream, static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H,
-                      groups, items, T * k, err_word);
+    auto kern = dispatch_fp8_kernel<QUANT_U, COAL>;
+    const int grid = warp_item_grid((const void *)kern, DISPATCH_THREADS, 0, items);
+    return launch_pdl(kern, dim3(grid), dim3(DISPATCH_THREADS), 0, stream,
+                      static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H, groups,
+                      items, rows, err_word);
+}
+
+cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
+                                uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
+                                cudaStream_t stream)
+{
+    return launch_fp8<false>(T, H, k, x, slot_of, recv_q, recv_scales, T * k, err_word, stream);
+}
+
+cudaError_t launch_dispatch_fp8_coalesced(int T, int H, int k, const void *x,
+                                          const int32_t *crow, uint8_t *recv_q,
+                                          float *recv_scales, int rows, uint32_t *err_word,
+                                          cudaStream_t stream)
+{
+    return launch_fp8<true>(T, H, k, x, crow, recv_q, recv_scales, rows, err_word, stream);
 }
 
 }  // namespace moe

@@ -40,6 +40,11 @@ cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_
                                 uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
                                 cudaStream_t stream);
 
+cudaError_t launch_dispatch_fp8_coalesced(int T, int H, int k, const void *x,
+                                          const int32_t *crow, uint8_t *recv_q,
+                                          float *recv_scales, int rows, uint32_t *err_word,
+                                          cudaStream_t stream);
+
 cudaError_t launch_combine(int T, int H, int k, const void *y, const int32_t *slot_of,
                            const float *topk_w, void *out, bool out_f32,
                            uint32_t *err_word, cudaStream_t stream);

@@ -287,6 +287,25 @@ MOE_API moe_status moe_dispatch_coalesced(int T, int H, int k, const void *x,
                                   uint32_t *err_word, cudaStream_t stream);
 
 /*
+ * moe_dispatch_quant_coalesced -- moe_dispatch_quant into the rank-coalesced
+ * rows: each token's E4M3 codes and fp32 scales (the moe_dispatch_quant
+ * reading: 1x128 blocks, scale = amax / 448) are written once per distinct
+ * destination rank.
+ *
+ * RailWave, section 3.1 (token coalescing); UBEP, Table 3 (W8A8).
+ *   crow        [T, k]         from moe_layout_coalesced
+ *   rows        capacity of the outputs in rows (as for moe_dispatch_coalesced)
+ *   recv_q      [rows, H]      out: E4M3 codes (16-byte aligned)
+ *   recv_scales [rows, H/128]  out: fp32 scales (16-byte aligned)
+ * 1 <= k <= 32 (larger k: MOE_ERR_UNSUPPORTED); H % 128 == 0.  Row indices
+ * outside [0, rows) set MOE_ERRBIT_BAD_INDEX and are skipped.
+ */
+MOE_API moe_status moe_dispatch_quant_coalesced(int T, int H, int k, const void *x,
+                                        const int32_t *crow, int rows, uint8_t *recv_q,
+                                        float *recv_scales, uint32_t *err_word,
+                                        cudaStream_t stream);
+
+/*
  * moe_combine_coalesced -- the return path of the coalesced dispatch: each
  * destination rank pre-reduces a token's slots it holds into the token's
  * coalesced row, then the token sums its rows.

@@ -149,3 +149,7 @@ def test_coalesced_calls_reject_bad_arguments(m):
     assert L.moe_combine_coalesced(4, 64, 2, *cargs, FAKE + 8, FAKE, 0, None, None) == bad
     assert L.moe_combine_coalesced(4, 64, 2, FAKE, FAKE, FAKE, FAKE, -1, FAKE, FAKE, 0, None,
                                    None) == bad
+    # coalesced FP8 dispatch: H % 128, k above 32
+    assert L.moe_dispatch_quant_coalesced(4, 192, 2, FAKE, FAKE, 8, FAKE, FAKE, None, None) == bad
+    assert L.moe_dispatch_quant_coalesced(4, 256, 40, FAKE, FAKE, 8, FAKE, FAKE, None,
+                                          None) == m.MOE_ERR_UNSUPPORTED

@@ -273,3 +273,26 @@ def test_coalesced_combine_empty_and_bad_rows():
     wt = torch.ones((3, 2), dtype=torch.float32, device="cuda")
     m.moe_combine_coalesced(y, lay.slot_of, wt, co, 3, err_word=err)
     assert m.moe_read_error(err) == m.MOE_ERRBIT_BAD_INDEX
+
+
+
+# ------------------------------------------------------------ FP8 dispatch
+
+@pytest.mark.parametrize("name", ["dsv3_prefill", "tiny", "dsv3_decode"])
+def test_coalesced_dispatch_quant_matches_oracle(name):
+    """Each coalesced row holds the token's codes and scales, as the plain
+    FP8 dispatch writes them to every slot of that token."""
+    m = cl()
+    w = workload(name)
+    lay, co, nc = assert_coalesced_equal(w.topk_idx, w.E, w.R)
+    rows = w.T * min(w.k, w.R)
+    q = torch.full((rows, w.H), 0x5A, dtype=torch.uint8, device="cuda")
+    sc = torch.full((rows, w.H // 128), -1.0, dtype=torch.float32, device="cuda")
+    m.moe_dispatch_quant_coalesced(bf16_dev(w.x), co.crow, rows, recv_q=q, recv_scales=sc)
+    slot_of = lay.slot_of.cpu().numpy()
+    rq, rs = oracle.dispatch_quant(w.x, slot_of)
+    src = co.src_pair_c.cpu().numpy()[:nc]
+    owner_slot = slot_of.ravel()[src]
+    assert np.array_equal(q.cpu().numpy()[:nc], rq[owner_slot])
+    assert np.array_equal(sc.cpu().numpy()[:nc], rs[owner_slot])
+    assert (q.cpu().numpy()[nc:] == 0x5A).all() and (sc.cpu().numpy()[nc:] == -1.0).all()
