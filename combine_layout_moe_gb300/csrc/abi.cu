@@ -1,6 +1,7 @@
 // C ABI entry points of libmoe_ep.so: argument checks, then the launchers.
 // Nothing here allocates device memory or synchronises, except
 // moe_read_error, whose job is to synchronise and read the error word.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -9,19 +10,24 @@
 
 namespace moe {
 
+// SM count of the current device, cached per device (any host thread may call
+// the library; every thread that fills an entry writes the same value).
 int sm_count()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return 1;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0)
-        return cached[dev];
+    if (dev >= 0 && dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0)
+            return c;
+    }
     int n = 1;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
         n = 1;
     if (dev >= 0 && dev < 64)
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
