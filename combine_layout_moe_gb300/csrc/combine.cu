@@ -11,8 +11,9 @@
 // CH bytes of each of its k source rows (k * CH ~ 32 KB, equal chunks).  A
 // producer warp issues one cp.async.bulk per source row chunk into a ring of 6
 // shared-memory stages, completing on the stage's "full" mbarrier, and writes
-// the token's weights and valid-slot mask into the stage header; consumer
-// warps wait on it, fold the k chunks into fp32 accumulators with one fused
+// the token's weights and valid-slot mask into the stage header; the stage's
+// consumer warps (one group of up to three per stage, splitting its 16-byte
+// vectors) wait on it, fold the k chunks into fp32 accumulators with one fused
 // multiply-add per slot in slot order j = 0..k-1 (starting from +0), round
 // once (nearest-even), store 16-byte vectors, and release the stage through
 // its "empty" mbarrier.  The SM keeps up to ~190 KB of reads in flight without
@@ -131,8 +132,16 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2)
 #ifndef MOE_CT_STAGE_TARGET
 #define MOE_CT_STAGE_TARGET 32768
 #endif
+#ifndef MOE_CT_MAX_WPS
+#define MOE_CT_MAX_WPS 3
+#endif
+// CT_CONSUMERS consumer groups own the stages (stage s belongs to group
+// s % CT_CONSUMERS); each group has `wps` warps (a launch argument, at most
+// CT_MAX_WPS) that split a stage's 16-byte vectors between them, so a landed
+// stage is folded and released sooner.
 constexpr int CT_CONSUMERS = MOE_CT_CONSUMERS;
-constexpr int CT_THREADS = 32 * (CT_CONSUMERS + 1);
+constexpr int CT_MAX_WPS = MOE_CT_MAX_WPS;
+constexpr int CT_MAX_THREADS = 32 * (CT_CONSUMERS * CT_MAX_WPS + 1);
 constexpr int CT_STAGES = MOE_CT_STAGES;
 constexpr int CT_STAGE_TARGET = MOE_CT_STAGE_TARGET;  // bytes of k row chunks per stage
 // Stage header words: [0, 32) slot weights, 32 valid-slot mask, 33 group-leader
@@ -142,7 +151,7 @@ constexpr int CT_HDR_OK = 32, CT_HDR_LEAD = 33, CT_HDR_MEMB = 36, CT_HDR_ROW = 6
 constexpr int CT_BAR_BYTES = 16 * CT_STAGES;
 constexpr int CT_HDR_BYTES = 4 * CT_HDR_WORDS * CT_STAGES;
 constexpr int CT_PREFIX = (CT_BAR_BYTES + CT_HDR_BYTES + 127) / 128 * 128;
-static_assert(CT_STAGES % CT_CONSUMERS == 0, "each consumer warp owns whole stages");
+static_assert(CT_STAGES % CT_CONSUMERS == 0, "each consumer group owns whole stages");
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
@@ -211,12 +220,12 @@ __device__ __forceinline__ void store_row8(void *out, int out_f32, int64_t e0, c
 enum { CB_PLAIN = 0, CB_COAL = 1 };
 
 template <int KMAX, int MODE>
-__global__ void __launch_bounds__(CT_THREADS, 1)
+__global__ void __launch_bounds__(CT_MAX_THREADS, 1)
     combine_bulk_kernel(const uint8_t *__restrict__ y, const int32_t *__restrict__ slot_of,
                         const float *__restrict__ topk_w, const int32_t *__restrict__ crow,
                         void *__restrict__ part, void *__restrict__ out, int out_f32, int T,
                         int H, int k, int bound, int gbound, int CH, int nchunks, int64_t units,
-                        uint32_t *err_word)
+                        int wps, uint32_t *err_word)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t bars = smem_addr(smem);
@@ -231,7 +240,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < CT_STAGES; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 1);
+            mbar_init(empty(s), (uint32_t)wps);
         }
         mbar_fence_init();
     }
@@ -335,8 +344,10 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
         return;
     }
 
-    // ---------------- consumers: unit n goes to warp 1 + n % CT_CONSUMERS
-    const int cw = warp - 1;
+    // ---------------- consumers: unit n goes to group n % CT_CONSUMERS, whose
+    // wps warps take every wps-th vector of it
+    const int cw = (warp - 1) % CT_CONSUMERS;
+    const int sub = (warp - 1) / CT_CONSUMERS;
     int64_t t = (u0 + cw) / nchunks;
     int c = (int)(u0 + cw - t * nchunks);
     for (int64_t n = cw; n < nloc; n += CT_CONSUMERS) {
@@ -349,7 +360,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                 report(err_word, MOE_ERRBIT_TIMEOUT);
             return;
         }
-        if (n == 0 && lane == 0)
+        if (n == 0 && sub == 0 && lane == 0)
             CT_TRACE(1);
         const float *h = hdr + s * CT_HDR_WORDS;
         const unsigned okmask = reinterpret_cast<const uint32_t *>(h)[CT_HDR_OK];
@@ -366,7 +377,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
             const uint32_t *hu = reinterpret_cast<const uint32_t *>(h);
             const unsigned leaders = hu[CT_HDR_LEAD];
             const int64_t col0 = (int64_t)c * (CH / 2);
-            for (int v = lane; v < cb / 16; v += 32) {
+            for (int v = lane + 32 * sub; v < cb / 16; v += 32 * wps) {
                 float tot[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -405,7 +416,7 @@ __global__ void __launch_bounds__(CT_THREADS, 1)
                 store_row8(out, out_f32, out_elem0 + (int64_t)v * 8, tot);
             }
         } else {
-            for (int v = lane; v < cb / 16; v += 32) {
+            for (int v = lane + 32 * sub; v < cb / 16; v += 32 * wps) {
                 float acc[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -458,21 +469,31 @@ static cudaError_t launch_combine_bulk(int T, int H, int k, const void *y,
     nchunks = (rowbytes + CH - 1) / CH;
     const int64_t units = (int64_t)T * nchunks;
     const size_t smem = CT_PREFIX + (size_t)CT_STAGES * k * CH;
+    // Consumer warps per stage.  Splitting a stage over three warps folds and
+    // releases it sooner (measured, one GB300, each combine after a flush:
+    // 1024 tokens, H = 7168, k = 8: 29.9 -> 27.2 us; 8192 tokens: 178 -> 166 us;
+    // coalesced 1024 tokens: 60.0 -> 41.5 us).  The plain combine of k <= 2
+    // keeps one warp per stage: its producer issues a unit every 2 rows and
+    // loses issue slots to the extra warps (65536 tokens, H = 4096, k = 2:
+    // 240 us with one warp, 280 us with three).
+    const int wps = (MODE == CB_PLAIN && k <= 2) ? 1 : CT_MAX_WPS;
+    const int threads = 32 * (CT_CONSUMERS * wps + 1);
     auto kern = combine_bulk_kernel<KMAX, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess)
         return e;
     int per_sm = 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CT_THREADS, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) !=
             cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const int64_t g = units < cap ? units : cap;
-    return launch_pdl(kern, dim3((unsigned)g), dim3(CT_THREADS), smem, stream,
+    return launch_pdl(kern, dim3((unsigned)g), dim3(threads), smem, stream,
                       static_cast<const uint8_t *>(y), slot_of, topk_w, crow, part, out,
-                      out_f32 ? 1 : 0, T, H, k, bound, gbound, CH, nchunks, units, err_word);
+                      out_f32 ? 1 : 0, T, H, k, bound, gbound, CH, nchunks, units, wps,
+                      err_word);
 }
 
 template <int KC, int U>
