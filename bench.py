@@ -58,9 +58,13 @@ def kernel_bytes(name: str, T: int, H: int, k: int, E: int, R: int = 1) -> int:
 
     layout_count   reads topk_idx once
     layout_assign  reads topk_idx, writes slot_of and src_of, counts and offsets
+    layout_dispatch  both of the above
     dispatch_bf16  reads x and slot_of once, writes k copies of every row
     dispatch_fp8   reads x and slot_of, writes k copies of the codes and scales
     combine        reads k rows per token, slot_of and weights, writes one row
+    combine_backward  reads dout and the k rows of y, writes the k rows of dy
+                   and dw
+    dispatch_backward  reads the k rows of drecv per token, writes dx
     The coalesced kernels also depend on Nc, the number of coalesced rows:
     dispatch_coalesced  reads x and crow, writes Nc rows
     dispatch_fp8_coalesced  reads x and crow, writes Nc rows of codes and scales
@@ -78,6 +82,12 @@ def kernel_bytes(name: str, T: int, H: int, k: int, E: int, R: int = 1) -> int:
         return 2 * T * H + 4 * N + N * H + 4 * N * (H // 128)
     if name == "combine":
         return 2 * N * H + 8 * N + 2 * T * H
+    if name == "layout_dispatch":
+        return 12 * N + 4 * (2 * E + 1 + R + 1) + 2 * T * H + 4 * N + 2 * N * H
+    if name == "combine_backward":   # reads dout, k rows of y, slot_of, w; writes dy, dw
+        return 2 * T * H + 2 * N * H + 2 * N * H + 12 * N
+    if name == "dispatch_backward":  # the unit-weight combine of drecv
+        return 2 * N * H + 4 * N + 2 * T * H
     raise KeyError(name)
 
 
@@ -89,6 +99,8 @@ def coalesced_bytes(name: str, T: int, H: int, k: int, Nc: int) -> int:
         return 2 * T * H + 4 * N + Nc * H + 4 * Nc * (H // 128)
     if name == "combine_coalesced":
         return 2 * N * H + 12 * N + 2 * Nc * H + 2 * T * H
+    if name == "layout_coalesced":  # reads ids and slot_of; writes crow, src_pair_c, expand
+        return 20 * N
     raise KeyError(name)
 
 
@@ -629,6 +641,132 @@ def run_gpu(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ kernel table
+
+def run_table(args):
+    """Every entry point alone, on every workload: each launch follows a write
+    of 2xL2 and a read of 4xL2 (cold, clean L2), bracketed by CUDA events on
+    its stream; 5 warm-ups, then args.table_reps launches.  Prints one JSON
+    line per (workload, kernel): median and minimum time, algorithmic bytes,
+    achieved GB/s and the fraction of the measured HBM peak."""
+    import torch
+    import combine_layout_moe_gb300 as m
+    from workloads.gen import make_workload, expert_output, CONFIGS, CONFIG_ORDER
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    fw = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    fr = torch.zeros(max(4 * l2, 512 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = measured_peak_gbs()
+    names = CONFIG_ORDER if args.table_all else [args.config]
+    for name in names:
+        w = make_workload(name)
+        T, H, k, E, R, N = w.T, w.H, w.k, w.E, w.R, w.N
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)  # noqa: E731
+        x, y = bf(w.x), bf(expert_output(N, H, seed=w.seed))
+        dout = bf(expert_output(T, H, seed=w.seed + 1))
+        idx = torch.from_numpy(w.topk_idx).to(dev)
+        wt = torch.from_numpy(w.topk_w).to(dev)
+        err = m.new_error_word(dev)
+        ws = m.new_workspace(m.moe_layout_workspace_bytes(T, k, E), dev)
+        wsc = m.new_workspace(m.moe_layout_workspace_bytes(T, k, R), dev)
+        lay = m.moe_layout(idx, E, R, workspace=ws, err_word=err)
+        co = m.moe_layout_coalesced(idx, lay.slot_of, E, R, workspace=wsc, err_word=err)
+        torch.cuda.synchronize()
+        Nc = int(co.rank_offsets_c[R].item())
+        rows = T * min(k, R)
+        recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        rq = torch.empty((N, H), dtype=torch.uint8, device=dev)
+        rs = torch.empty((N, H // 128), dtype=torch.float32, device=dev)
+        rc = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        part = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        dy = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        dw = torch.empty((T, k), dtype=torch.float32, device=dev)
+        kw = dict(err_word=err, stream=stream)
+        ops = [
+            ("layout", lambda: m.moe_layout(idx, E, R, workspace=ws, out=lay, **kw),
+             kernel_bytes("layout_assign", T, H, k, E, R)),
+            ("layout_dispatch", lambda: m.moe_layout_dispatch(x, idx, E, R, workspace=ws, out=lay,
+                                                              recv=recv, **kw),
+             kernel_bytes("layout_dispatch", T, H, k, E, R)),
+            ("dispatch_bf16", lambda: m.moe_dispatch(x, lay.slot_of, recv=recv, **kw),
+             kernel_bytes("dispatch_bf16", T, H, k, E, R)),
+            ("combine", lambda: m.moe_combine(y, lay.slot_of, wt, out=out, **kw),
+             kernel_bytes("combine", T, H, k, E, R)),
+            ("combine_backward", lambda: m.moe_combine_backward(dout, y, lay.slot_of, wt, dy=dy,
+                                                                dw=dw, **kw),
+             kernel_bytes("combine_backward", T, H, k, E, R)),
+            ("dispatch_backward", lambda: m.moe_dispatch_backward(y, lay.slot_of, dx=out, **kw),
+             kernel_bytes("dispatch_backward", T, H, k, E, R)),
+            ("layout_coalesced", lambda: m.moe_layout_coalesced(idx, lay.slot_of, E, R,
+                                                                workspace=wsc, out=co, **kw),
+             coalesced_bytes("layout_coalesced", T, H, k, Nc)),
+            ("dispatch_coalesced", lambda: m.moe_dispatch_coalesced(x, co.crow, rows, recv_c=rc,
+                                                                    **kw),
+             coalesced_bytes("dispatch_coalesced", T, H, k, Nc)),
+            ("combine_coalesced", lambda: m.moe_combine_coalesced(y, lay.slot_of, wt, co, rows,
+                                                                  partial=part, out=out, **kw),
+             coalesced_bytes("combine_coalesced", T, H, k, Nc)),
+        ]
+        if H % 128 == 0:
+            ops.insert(3, ("dispatch_fp8", lambda: m.moe_dispatch_quant(x, lay.slot_of, recv_q=rq,
+                                                                        recv_scales=rs, **kw),
+                           kernel_bytes("dispatch_fp8", T, H, k, E, R)))
+            ops.insert(-1, ("dispatch_fp8_coalesced",
+                            lambda: m.moe_dispatch_quant_coalesced(x, co.crow, rows, recv_q=rq,
+                                                                   recv_scales=rs, **kw),
+                            coalesced_bytes("dispatch_fp8_coalesced", T, H, k, Nc)))
+        if args.table_flagged:
+            # A7: dispatch -> identity expert -> combine in one kernel, per
+            # readiness mode and granularity, against the same three steps as
+            # separate launches (the expert is torch's copy of recv into y)
+            yf = torch.empty_like(y)
+            nb_f = 4 * T * H + 8 * N * H
+            ops = [("separate", lambda: (m.moe_dispatch(x, lay.slot_of, recv=recv, **kw),
+                                         yf.copy_(recv),
+                                         m.moe_combine(yf, lay.slot_of, wt, out=out, **kw)), nb_f)]
+            for mode, grans in ((m.MOE_SYNC_BARRIER, (2048,)), (m.MOE_SYNC_BATCH, (2048, 4096, 8192)),
+                                (m.MOE_SYNC_WORD, (2048, 4096, 8192)), (m.MOE_SYNC_SENTINEL, (2048,))):
+                for g in grans:
+                    label = {m.MOE_SYNC_BARRIER: "barrier", m.MOE_SYNC_BATCH: f"batch_{g}",
+                             m.MOE_SYNC_WORD: f"word_{g}", m.MOE_SYNC_SENTINEL: "sentinel"}[mode]
+                    ops.append((f"flagged_{label}", (mode, g), nb_f))
+        for op, fn, nbytes in ops:
+            state = None
+            if isinstance(fn, tuple):
+                state = m.SyncState(T, H, k, fn[0], fn[1], device=dev)
+                fn = (lambda st: lambda: m.moe_dispatch_combine_flagged(x, lay.slot_of, wt, st,
+                                                                         out=out, **kw))(state)
+            evs = []
+            for i in range(5 + args.table_reps):
+                fw.fill_(0)
+                fr.view(torch.int64).sum()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                if i >= 5:
+                    evs.append((a, b))
+            torch.cuda.synchronize()
+            us = sorted(a.elapsed_time(b) * 1000.0 for a, b in evs)
+            med = statistics.median(us)
+            bits = m.moe_read_error(err)
+            if bits:
+                raise RuntimeError(f"device error bits {bits:#x} in {name}/{op}")
+            gbs = nbytes / (med * 1e-6) / 1e9
+            del state
+            print(json.dumps({"workload": name, "kernel": op, "median_us": round(med, 2),
+                              "min_us": round(us[0], 2), "algorithmic_bytes": nbytes,
+                              "gbs": round(gbs, 1), "frac": round(gbs / peak, 3),
+                              "peak": f"{peak_kind} hbm_gbs {peak}",
+                              "rows": {"N": N, "Nc": Nc}}), flush=True)
+        del x, y, dout, recv, rq, rs, rc, part, out, dy, ops
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -644,10 +782,20 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--variant", choices=["plain", "coalesced"], default="plain",
                    help="plain: the hot path; coalesced: the rank-coalesced path")
+    p.add_argument("--table", action="store_true",
+                   help="time every entry point alone after a flush (one JSON line each) "
+                        "on --config, or on every workload with --table-all")
+    p.add_argument("--table-all", action="store_true")
+    p.add_argument("--table-flagged", action="store_true",
+                   help="with --table: the single-kernel Data-as-Flag variant per readiness "
+                        "mode and granularity, against separate launches")
+    p.add_argument("--table-reps", type=int, default=50)
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.table or args.table_all or args.table_flagged:
+        run_table(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
