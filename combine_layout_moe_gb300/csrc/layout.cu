@@ -13,6 +13,11 @@
 //      expert ids stay in registers); the CTA writes the row sums to its row of
 //      the tile-count table.
 //   2. Grid barrier (arrival count and generation in the workspace; bounded).
+//      With at most CLUSTER_MAX_TILES tiles the grid is one thread-block
+//      cluster instead: each CTA keeps its row in shared memory, a hardware
+//      cluster barrier replaces the grid barrier, and step 3 reads the other
+//      CTAs' rows through distributed shared memory (no table in global
+//      memory, no atomics, no polling).
 //   3. Each CTA column-sums the table (all tiles -> totals -> exclusive scan
 //      over experts; earlier tiles -> this tile's base), turns the per-warp
 //      histograms into per-warp cursors, and walks its span in order:
@@ -40,6 +45,23 @@ constexpr int LAYOUT_MAX_TILES = 128;     // bounds the tile-count table each CT
 constexpr int LAYOUT_BATCH = 8;           // expert ids loaded ahead per lane
 constexpr int TABLE_UNROLL = 8;           // independent table loads in flight per thread
 constexpr size_t LAYOUT_BARRIER_BYTES = 256;  // workspace head: grid-barrier count and generation
+constexpr int CLUSTER_MAX_TILES = 8;          // portable thread-block cluster size
+
+// Thread-block cluster barrier, split into its arrive (release) and wait
+// (acquire) halves; every thread of every CTA of the cluster takes part.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// 32-bit load from the shared memory of CTA `rank` of this cluster, at the
+// offset that `local` (a shared-memory address of this CTA) has here.
+__device__ __forceinline__ int32_t ld_dsmem_s32(uint32_t local, uint32_t rank)
+{
+    uint32_t remote;
+    int32_t v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
 
 // Out-of-span lanes carry NO_PAIR; pairs with an expert id outside [0, E) carry
 // BAD_PAIR (they get slot -1 and take no slot).  With COAL, a pair whose rank
@@ -121,7 +143,7 @@ template <int NBITS, bool COAL>
 __global__ void __launch_bounds__(LAYOUT_THREADS)
     layout_kernel(const int32_t *__restrict__ idx, int64_t N, int E, int R, int e_real, int El,
                   int k, int span,
-                  int tiles, unsigned *barrier, int32_t *tile_counts,
+                  int tiles, int cluster, unsigned *barrier, int32_t *tile_counts,
                   int32_t *__restrict__ expert_counts, int32_t *__restrict__ expert_offsets,
                   int32_t *__restrict__ rank_offsets, int32_t *__restrict__ slot_of,
                   int32_t *__restrict__ src_of, const int32_t *__restrict__ plain_slot,
@@ -132,6 +154,7 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
     int32_t *offs = wcnt + LAYOUT_WARPS * E;  // [E]: totals, then exclusive offsets
     int32_t *pre = offs + E;                  // [E]: pairs of e in earlier tiles
     int32_t *carry = pre + E;                 // [LAYOUT_WARPS]: scan of warp sums
+    int32_t *tsum = carry + LAYOUT_WARPS;     // [E]: this tile's counts (cluster path)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < LAYOUT_WARPS * E + 2 * E; i += LAYOUT_THREADS)
@@ -184,18 +207,45 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
 #pragma unroll 4
             for (int w = 0; w < LAYOUT_WARPS; ++w)
                 s += wcnt[w * E + e];
-            tile_counts[(int64_t)blockIdx.x * E + e] = s;
+            if (cluster)
+                tsum[e] = s;
+            else
+                tile_counts[(int64_t)blockIdx.x * E + e] = s;
         }
 
         LAYOUT_TRACE(2);
         // 2. every tile row is written
-        if (!grid_barrier(barrier, err_word))
+        if (cluster) {
+            cluster_arrive();
+            cluster_wait();
+        } else if (!grid_barrier(barrier, err_word)) {
             return;
+        }
         LAYOUT_TRACE(3);
     }
 
     // 3a. column sums of the table; thread (part, e) sums rows part, part+P, ...
-    if (tiles > 1) {
+    if (tiles > 1 && cluster) {
+        // the rows are the cluster's tsum arrays (CTA rank = tile); only ranks
+        // that exist are read, and a cluster of another size is reported
+        uint32_t ncta;
+        asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
+        const int nread = min(tiles, (int)ncta);
+        if (tid == 0 && (int)ncta != tiles)
+            report(err_word, MOE_ERRBIT_TIMEOUT);
+        for (int e = tid; e < E; e += LAYOUT_THREADS) {
+            const uint32_t la = smem_addr(tsum + e);
+            int32_t before = 0, total = 0;
+            for (int b = 0; b < nread; ++b) {
+                const int32_t v = ld_dsmem_s32(la, (uint32_t)b);
+                total += v;
+                before += b < (int)blockIdx.x ? v : 0;
+            }
+            offs[e] = total;
+            pre[e] = before;
+        }
+        cluster_arrive();  // done reading the other CTAs' shared memory
+    } else if (tiles > 1) {
         const int P = E >= LAYOUT_THREADS ? 1 : LAYOUT_THREADS / E;
         const int part = tid / E;
         for (int e = tid % E; part < P && e < E; e += LAYOUT_THREADS) {
@@ -332,6 +382,8 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
         }
     }
     LAYOUT_TRACE(7);
+    if (tiles > 1 && cluster)
+        cluster_wait();  // no CTA leaves while another may still read its tsum
 }
 
 // ---------------------------------------------------------------- host side
@@ -360,7 +412,7 @@ static LayoutPlan layout_plan(int64_t N)
 
 static size_t layout_smem(int E)
 {
-    return sizeof(int32_t) * ((size_t)LAYOUT_WARPS * E + 2 * (size_t)E + LAYOUT_WARPS);
+    return sizeof(int32_t) * ((size_t)LAYOUT_WARPS * E + 3 * (size_t)E + LAYOUT_WARPS);
 }
 
 size_t layout_workspace_bytes(int64_t N, int E)
@@ -387,32 +439,48 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, 
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    // Cooperative: all CTAs are co-resident, as the grid barrier requires.
-    // Programmatic serialisation: the grid may become resident while the
-    // previous kernel in the stream finishes.
+    // One cluster (at most CLUSTER_MAX_TILES CTAs): the cluster barrier and
+    // distributed shared memory replace the table and the grid barrier.
+    // Otherwise cooperative: all CTAs are co-resident, as the grid barrier
+    // requires.  Either way with programmatic serialisation: the grid may
+    // become resident while the previous kernel in the stream finishes.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.tiles);
     cfg.blockDim = dim3(LAYOUT_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS, COAL>, topk_idx, N, E, R, e_real, El, k,
-                           p.span, p.tiles, barrier, tile_counts, expert_counts, expert_offsets,
-                           rank_offsets, slot_of, src_of, plain_slot, expand, err_word);
+    auto launch = [&](int cluster, int nattr) {
+        cfg.numAttrs = nattr;
+        return cudaLaunchKernelEx(&cfg, layout_kernel<NBITS, COAL>, topk_idx, N, E, R, e_real,
+                                  El, k, p.span, p.tiles, cluster, barrier, tile_counts,
+                                  expert_counts, expert_offsets, rank_offsets, slot_of, src_of,
+                                  plain_slot, expand, err_word);
+    };
+    if (p.tiles > 1 && p.tiles <= CLUSTER_MAX_TILES) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)p.tiles;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        e = launch(1, 2);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            e = launch(1, 1);  // without the programmatic attribute
+        }
+        if (e == cudaSuccess)
+            return e;
+        (void)cudaGetLastError();  // no cluster of this size: the cooperative form below
+    }
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    e = launch(0, 2);
     if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
         // the driver refused the attribute pair: launch cooperatively only
         (void)cudaGetLastError();
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, layout_kernel<NBITS, COAL>, topk_idx, N, E, R, e_real, El, k,
-                               p.span, p.tiles, barrier, tile_counts, expert_counts,
-                               expert_offsets, rank_offsets, slot_of, src_of, plain_slot,
-                               expand, err_word);
+        e = launch(0, 1);
     }
     return e;
 }

@@ -78,6 +78,9 @@ FUZZ = [  # (seed, T, k, E, R)
     (6, 257, 4, 256, 32), (7, 4097, 3, 5, 5), (8, 5000, 8, 1024, 8), (9, 12345, 6, 64, 16),
     (10, 70000, 2, 2, 2), (11, 100000, 8, 128, 16), (12, 300000, 8, 256, 32),
     (13, 2049, 1, 3, 1), (14, 511, 16, 40, 10), (15, 40, 33, 9, 3),
+    # around the one-cluster form (at most 8 tiles of ~1024 pairs): 8000 pairs
+    # with the largest expert count, 8192 pairs (8 tiles), 8193 pairs (9 tiles)
+    (16, 1000, 8, 1024, 8), (17, 4096, 2, 32, 4), (18, 8193, 1, 64, 4),
 ]
 
 
@@ -112,16 +115,17 @@ def test_layout_empty():
     assert lay.rank_offsets.cpu().tolist() == [0] * 3
 
 
-def test_layout_bad_index_reported():
+@pytest.mark.parametrize("T", [64, 2048, 20000])   # one tile, one cluster, the grid barrier
+def test_layout_bad_index_reported(T):
     m = cl()
     err = m.new_error_word()
-    idx = np.zeros((64, 2), np.int32)
+    idx = np.zeros((T, 2), np.int32)
     idx[10, 1] = 8
-    idx[20, 0] = -3
+    idx[T - 20, 0] = -3
     m.moe_layout(i32_dev(idx), 8, 2, err_word=err)
     assert m.moe_read_error(err) & m.MOE_ERRBIT_BAD_INDEX
     assert m.moe_read_error(err) == 0          # cleared by the first read
-    m.moe_layout(i32_dev(np.zeros((64, 2), np.int32)), 8, 2, err_word=err)
+    m.moe_layout(i32_dev(np.zeros((T, 2), np.int32)), 8, 2, err_word=err)
     assert m.moe_read_error(err) == 0
 
 
