@@ -513,8 +513,10 @@ static cudaError_t launch_combine_t(int T, int H, int k, const void *y, const in
 // ---------------------------------------------------------------- backward
 //
 // HyperParallel-MoE, section 2.2 / Figure 2(b): the backward Dispatch is the
-// gradient of the forward Combine.  One CTA per token: its 8 warps take equal
-// slices of the row; per 16-byte vector a lane loads dout and the k rows of y
+// gradient of the forward Combine.  Three forms: a warp per token for k <= 4,
+// the bulk-copy pipeline below for 5 <= k <= 8, and for larger k (or when the
+// pipeline does not fit in shared memory) one CTA per token: its 8 warps take
+// equal slices of the row; per 16-byte vector a lane loads dout and the k rows of y
 // (KMAX / 8 groups of 8 loads in flight), stores the k scaled copies
 // dy[slot_of[t,j]] = bf16(w[t,j] * dout[t]) (one fp32 multiply, one rounding)
 // and accumulates the k dot products <y[slot_of[t,j]], dout[t]> in fp32.  The
@@ -793,6 +795,325 @@ static cudaError_t launch_combine_backward_warp(int T, int H, int k, const void 
                       topk_w, static_cast<uint4 *>(dy), dw, T, k, H / 8, 1, err_word);
 }
 
+// ------------------------------------------------- backward through bulk copies
+//
+// The same gradient as combine_backward_kernel, on the forward combine's
+// pipeline: one persistent CTA per SM over a contiguous range of units (unit =
+// token t, chunk c of CH bytes).  The producer warp loads dout[t]'s chunk and
+// the k chunks of y[slot_of[t, j]] into a stage (one cp.async.bulk each) and
+// writes the weights and slots into its header; the stage's consumer group
+// stores dy[slot_of[t, j]] = bf16(w[t, j] * dout[t]) for its chunk and folds
+// the k dot-product partials of the chunk (per lane, then the group's warps in
+// index order).
+//
+// dw without a workspace, deterministic: each unit's k partials go to a small
+// shared-memory ring indexed by token; the group that completes a token's last
+// chunk in this CTA sums the token's chunk partials in chunk order and adds
+// the sum to dw, which the launch zero-fills.  The grid is at most T CTAs, so a
+// token's units lie in at most two CTAs: dw gets at most two additions onto
+// zero, and fp32 addition of two values does not depend on their order.  A
+// ring slot is reused by token t + CB_RING only after every unit of token t
+// was released (the finalisation precedes the release, and the producer
+// refills a stage only after its release), which CB_RING >= CT_STAGES makes
+// sufficient.  The same release order protects a group's reduction slots and
+// counter: its next unit's stage is refilled only after the group's last warp
+// has read them and arrived.
+constexpr int CB_RING = 8;
+static_assert(CB_RING >= CT_STAGES, "ring covers the units in flight");
+constexpr int CB_HDR_WORDS = 68;  // [0, 32) weights, [32, 64) slots, 64 valid-slot mask
+constexpr int CB_HDR_SLOT = 32, CB_HDR_OK = 64;
+
+template <int KMAX>
+__global__ void __launch_bounds__(CT_MAX_THREADS, 1)
+    combine_backward_bulk_kernel(const uint8_t *__restrict__ dout, const uint8_t *__restrict__ y,
+                                 const int32_t *__restrict__ slot_of,
+                                 const float *__restrict__ topk_w, uint8_t *__restrict__ dy,
+                                 float *__restrict__ dw, int T, int H, int k, int N, int CH,
+                                 int nchunks, int64_t units, int wps, uint32_t *err_word)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t bars = smem_addr(smem);
+    uint32_t *hdr = reinterpret_cast<uint32_t *>(smem + CT_BAR_BYTES);  // [CT_STAGES][CB_HDR_WORDS]
+    float *red = reinterpret_cast<float *>(hdr + CT_STAGES * CB_HDR_WORDS);  // [CT_CONSUMERS][CT_MAX_WPS][KMAX]
+    int32_t *gcnt = reinterpret_cast<int32_t *>(red + CT_CONSUMERS * CT_MAX_WPS * KMAX);  // [CT_CONSUMERS]
+    int32_t *cnt = gcnt + CT_CONSUMERS;                      // [CB_RING]
+    float *ring = reinterpret_cast<float *>(cnt + CB_RING);  // [CB_RING][nchunks][k]
+    const int ring_words = CB_RING * nchunks * k;
+    const uint32_t prefix =
+        (uint32_t)((CT_BAR_BYTES + 4 * (CT_STAGES * CB_HDR_WORDS + CT_CONSUMERS * CT_MAX_WPS * KMAX +
+                                        CT_CONSUMERS + CB_RING + ring_words) + 127) / 128 * 128);
+    const uint32_t stages = bars + prefix;
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (CT_STAGES + s); };
+    const bool want_dw = dw != nullptr && y != nullptr;
+    const uint32_t stage_bytes = (uint32_t)(want_dw ? 1 + k : 1) * CH;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t rowbytes = 2 * (int64_t)H;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < CT_STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), (uint32_t)wps);
+        }
+        mbar_fence_init();
+    }
+    for (int i = threadIdx.x; i < CT_CONSUMERS + CB_RING; i += blockDim.x)
+        gcnt[i] = 0;  // gcnt and cnt are contiguous
+    __syncthreads();
+    wait_prior_grid();
+    allow_next_grid();
+
+    const int64_t u0 = units * blockIdx.x / gridDim.x;
+    const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
+    const int64_t nloc = u1 - u0;
+    if (nloc <= 0)
+        return;
+    const int64_t t_first = u0 / nchunks;
+
+    if (warp == 0) {
+        // ---------------- producer
+        int64_t t = t_first;
+        int c = (int)(u0 - t * nchunks);
+        const bool kl = lane < k;
+        int32_t cur_s = kl ? ld_nc_s32(slot_of + t * k + lane) : -1;
+        float cur_w = kl ? ld_nc_f32(topk_w + t * k + lane) : 0.0f;
+        int32_t nxt_s = kl && t + 1 < T ? ld_nc_s32(slot_of + (t + 1) * k + lane) : -1;
+        float nxt_w = kl && t + 1 < T ? ld_nc_f32(topk_w + (t + 1) * k + lane) : 0.0f;
+        int64_t n = 0;
+        bool timed_out = false;
+        for (; n < nloc; ++n) {
+            if (n > 0 && ++c == nchunks) {
+                c = 0;
+                ++t;
+                cur_s = nxt_s;
+                cur_w = nxt_w;
+                nxt_s = kl && t + 1 < T ? ld_nc_s32(slot_of + (t + 1) * k + lane) : -1;
+                nxt_w = kl && t + 1 < T ? ld_nc_f32(topk_w + (t + 1) * k + lane) : 0.0f;
+            }
+            const int s = (int)(n % CT_STAGES);
+            const uint32_t r = (uint32_t)(n / CT_STAGES);
+            if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1)) {
+                timed_out = true;
+                break;
+            }
+            const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
+            const bool ok = kl && (unsigned)cur_s < (unsigned)N;
+            const unsigned okmask = __ballot_sync(FULL_MASK, ok);
+            uint32_t *h = hdr + s * CB_HDR_WORDS;
+            if (kl) {
+                h[lane] = __float_as_uint(cur_w);
+                h[CB_HDR_SLOT + lane] = (uint32_t)cur_s;
+            }
+            if (lane == 0)
+                h[CB_HDR_OK] = okmask;
+            __syncwarp();  // the header is written before lane 0 arrives
+            if (lane == 0) {
+                const unsigned kmask = k >= 32 ? FULL_MASK : (1u << k) - 1u;
+                if (c == 0 && okmask != kmask)
+                    report(err_word, MOE_ERRBIT_BAD_INDEX);
+                const uint32_t nrows = want_dw ? 1u + (uint32_t)__popc(okmask) : 1u;
+                mbar_arrive_expect_tx(full(s), nrows * cb);
+                bulk_g2s(stages + (uint32_t)s * stage_bytes,
+                         dout + t * rowbytes + (int64_t)c * CH, cb, full(s));
+            }
+            __syncwarp();
+            if (want_dw && ok)
+                bulk_g2s(stages + (uint32_t)s * stage_bytes + (uint32_t)(1 + lane) * CH,
+                         y + (int64_t)cur_s * rowbytes + (int64_t)c * CH, cb, full(s));
+        }
+        if (timed_out && lane == 0)
+            report(err_word, MOE_ERRBIT_TIMEOUT);
+        const int64_t first = n > CT_STAGES ? n - CT_STAGES : 0;
+        for (int64_t m = first + lane; m < n; m += 32) {
+            if (!mbar_wait(full((int)(m % CT_STAGES)), (uint32_t)(m / CT_STAGES) & 1))
+                report(err_word, MOE_ERRBIT_TIMEOUT);
+        }
+        return;
+    }
+
+    // ---------------- consumers: unit n goes to group n % CT_CONSUMERS
+    const int cw = (warp - 1) % CT_CONSUMERS;
+    const int sub = (warp - 1) / CT_CONSUMERS;
+    int64_t t = (u0 + cw) / nchunks;
+    int c = (int)(u0 + cw - t * nchunks);
+    for (int64_t n = cw; n < nloc; n += CT_CONSUMERS) {
+        if (n > cw)
+            advance(t, c, CT_CONSUMERS, nchunks);
+        const int s = (int)(n % CT_STAGES);
+        if (!mbar_wait(full(s), (uint32_t)(n / CT_STAGES) & 1)) {
+            if (lane == 0)
+                report(err_word, MOE_ERRBIT_TIMEOUT);
+            return;
+        }
+        const uint32_t *h = hdr + s * CB_HDR_WORDS;
+        const unsigned okmask = h[CB_HDR_OK];
+        float w[KMAX];
+        int32_t sl[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            w[j] = j < k ? __uint_as_float(h[j]) : 0.0f;
+            sl[j] = j < k ? (int32_t)h[CB_HDR_SLOT + j] : 0;
+        }
+        const int cb = (int)min((int64_t)CH, rowbytes - (int64_t)c * CH);
+        const uint32_t base = stages + (uint32_t)s * stage_bytes;
+        float part[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            part[j] = 0.0f;
+        for (int v = lane + 32 * sub; v < cb / 16; v += 32 * wps) {
+            const uint4 d = lds128(base + (uint32_t)v * 16);
+            const uint32_t d4[4] = {d.x, d.y, d.z, d.w};
+            float df[8];
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                df[2 * hh] = bf16lo(d4[hh]);
+                df[2 * hh + 1] = bf16hi(d4[hh]);
+            }
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (j >= k || !((okmask >> j) & 1u))
+                    continue;
+                uint32_t rr[4];
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(w[j], df[2 * hh]),
+                                                                   __fmul_rn(w[j], df[2 * hh + 1]));
+                    rr[hh] = *reinterpret_cast<const uint32_t *>(&b);
+                }
+                st_v4(dy + (int64_t)sl[j] * rowbytes + (int64_t)c * CH + (int64_t)v * 16,
+                      make_uint4(rr[0], rr[1], rr[2], rr[3]));
+                if (want_dw) {
+                    const uint4 q = lds128(base + (uint32_t)(1 + j) * CH + (uint32_t)v * 16);
+                    const uint32_t p[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        part[j] = __fmaf_rn(bf16lo(p[hh]), df[2 * hh], part[j]);
+                        part[j] = __fmaf_rn(bf16hi(p[hh]), df[2 * hh + 1], part[j]);
+                    }
+                }
+            }
+        }
+        if (want_dw) {
+            // the unit's partials: each warp's xor tree; the group's last warp
+            // to get here adds the warps' sums in index order and files them in
+            // the token's ring entry (no barrier: a warp that gives up on a
+            // wait cannot leave the others blocked)
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                float v = part[j];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1)
+                    v += __shfl_xor_sync(FULL_MASK, v, o);
+                part[j] = v;
+            }
+            float *rg = red + (cw * CT_MAX_WPS) * KMAX;
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j)
+                    rg[sub * KMAX + j] = part[j];
+            }
+            __syncwarp();
+            __threadfence_block();
+            int last = 0;
+            if (lane == 0)
+                last = atomicAdd(gcnt + cw, 1) + 1 == wps;
+            last = __shfl_sync(FULL_MASK, last, 0);
+            if (last) {
+                __threadfence_block();
+                const int ts = (int)((t - t_first) % CB_RING);
+                float *acc = ring + (ts * nchunks) * k;
+                if (lane < k) {
+                    float v = 0.0f;
+                    for (int q = 0; q < wps; ++q)
+                        v += rg[q * KMAX + lane];
+                    acc[c * k + lane] = v;
+                }
+                __syncwarp();
+                __threadfence_block();
+                int done = 0;
+                if (lane == 0) {
+                    gcnt[cw] = 0;
+                    const int64_t lo = max(u0, t * nchunks), hi = min(u1, (t + 1) * nchunks);
+                    done = atomicAdd(cnt + ts, 1) + 1 == (int)(hi - lo);
+                }
+                done = __shfl_sync(FULL_MASK, done, 0);
+                if (done) {
+                    // every chunk of token t in this CTA is filed: their sum in
+                    // chunk order
+                    __threadfence_block();
+                    const int c_lo = (int)(max(u0, t * nchunks) - t * nchunks);
+                    const int c_hi = (int)(min(u1, (t + 1) * nchunks) - t * nchunks);
+                    if (lane < k && ((okmask >> lane) & 1u)) {
+                        float v = 0.0f;
+                        for (int q = c_lo; q < c_hi; ++q)
+                            v += acc[q * k + lane];
+                        atomicAdd(dw + t * k + lane, v);
+                    }
+                    if (lane == 0)
+                        cnt[ts] = 0;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty(s));
+    }
+}
+
+// Returns cudaErrorNotSupported (nothing launched) when the ring and stages do
+// not fit in shared memory; the caller then takes the CTA-per-token kernel.
+template <int KMAX>
+static cudaError_t launch_combine_backward_bulk(int T, int H, int k, const void *dout,
+                                                const void *y, const int32_t *slot_of,
+                                                const float *topk_w, void *dy, float *dw,
+                                                uint32_t *err_word, cudaStream_t stream)
+{
+    const bool want_dw = dw != nullptr && y != nullptr;
+    const int rows = want_dw ? 1 + k : 1;  // chunks per stage: dout and the k rows of y
+    const int rowbytes = 2 * H;
+    const int vec = rowbytes / 16;
+    int nchunks = (int)(((int64_t)rowbytes * rows + CT_STAGE_TARGET - 1) / CT_STAGE_TARGET);
+    nchunks = max(1, min(nchunks, vec));
+    const int CH = (vec + nchunks - 1) / nchunks * 16;
+    nchunks = (rowbytes + CH - 1) / CH;
+    const int64_t units = (int64_t)T * nchunks;
+    // must match the kernel's layout: barriers, headers, reduction slots,
+    // group counters, ring counters, ring
+    const size_t prefix =
+        ((size_t)CT_BAR_BYTES + 4 * ((size_t)CT_STAGES * CB_HDR_WORDS + CT_CONSUMERS * CT_MAX_WPS * KMAX +
+                                     CT_CONSUMERS + CB_RING + (size_t)CB_RING * nchunks * k) + 127) /
+        128 * 128;
+    const size_t smem = prefix + (size_t)CT_STAGES * rows * CH;
+    int dev = 0, smem_max = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+        return cudaErrorNotSupported;
+    if (smem > (size_t)smem_max)
+        return cudaErrorNotSupported;
+    auto kern = combine_backward_bulk_kernel<KMAX>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    if (want_dw && (e = cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)T * k, stream)) !=
+                       cudaSuccess)
+        return e;
+    const int wps = CT_MAX_WPS;
+    const int threads = 32 * (CT_CONSUMERS * wps + 1);
+    // at most T CTAs: every CTA holds at least nchunks units, so a token's
+    // units lie in at most two CTAs (see above)
+    int64_t g = sm_count();
+    if (g > T)
+        g = T;
+    if (g > units)
+        g = units;
+    return launch_pdl(kern, dim3((unsigned)g), dim3(threads), smem, stream,
+                      static_cast<const uint8_t *>(dout), static_cast<const uint8_t *>(y),
+                      slot_of, topk_w, static_cast<uint8_t *>(dy), want_dw ? dw : nullptr, T, H,
+                      k, T * k, CH, nchunks, units, wps, err_word);
+}
+
 cudaError_t launch_combine_backward(int T, int H, int k, const void *dout, const void *y,
                                     const int32_t *slot_of, const float *topk_w, void *dy,
                                     float *dw, uint32_t *err_word, cudaStream_t stream)
@@ -805,9 +1126,16 @@ cudaError_t launch_combine_backward(int T, int H, int k, const void *dout, const
     if (k <= 4)
         return launch_combine_backward_warp<4, MOE_CBW4_UC, MOE_CBW4_MINB>(
             T, H, k, dout, y, slot_of, topk_w, dy, dw, err_word, stream);
-    if (k <= 8)
+    if (k <= 8) {
+        // the bulk-copy pipeline, unless its ring and stages do not fit (k > 8
+        // would hold 3 x k values per lane in registers: it spills)
+        const cudaError_t e = launch_combine_backward_bulk<8>(T, H, k, dout, y, slot_of, topk_w,
+                                                              dy, dw, err_word, stream);
+        if (e != cudaErrorNotSupported)
+            return e;
         return launch_combine_backward_t<8>(T, H, k, dout, y, slot_of, topk_w, dy, dw, err_word,
                                             stream);
+    }
     return launch_combine_backward_t<32>(T, H, k, dout, y, slot_of, topk_w, dy, dw, err_word,
                                          stream);
 }

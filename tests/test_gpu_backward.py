@@ -55,13 +55,17 @@ def _check_combine_backward(w, slot_of, y, dout):
     assert np.all(np.abs(got - rdw) <= bound), np.max(np.abs(got - rdw) - bound)
 
 
-@pytest.mark.parametrize("name", ["tiny", "dsv3_decode", "glm45_air", "mixtral"])
+@pytest.mark.parametrize("name", ["tiny", "dsv3_decode", "dsv3_prefill", "glm45_air", "mixtral"])
 def test_combine_backward_matches_oracle(name):
     _check_combine_backward(*_named(name))
 
 
+# 5 <= k <= 8 takes the bulk-copy pipeline: fewer tokens than SMs (one or a
+# few tokens per CTA), tokens split between two CTAs, k = 5..7, and one chunk
+# per row as well as many
 FUZZ = [(71, 1, 8, 1, 1, 1), (72, 33, 264, 3, 5, 5), (73, 100, 7176, 8, 16, 4),
-        (74, 17, 1024, 16, 20, 4), (75, 9, 512, 32, 40, 8)]
+        (74, 17, 1024, 16, 20, 4), (75, 9, 512, 32, 40, 8), (78, 777, 1000, 5, 10, 5),
+        (79, 7, 4096, 6, 12, 3), (80, 3001, 136, 7, 7, 7), (81, 1, 16384, 8, 8, 2)]
 
 
 @pytest.mark.parametrize("case", FUZZ, ids=[f"T{c[1]}_H{c[2]}_k{c[3]}" for c in FUZZ])
@@ -69,13 +73,25 @@ def test_combine_backward_fuzz(case):
     _check_combine_backward(*_fuzz(*case))
 
 
-def test_combine_backward_without_dw():
+@pytest.mark.parametrize("k", [4, 8])
+def test_combine_backward_without_dw(k):
     m = cl()
-    w, slot_of, y, dout = _fuzz(76, 40, 256, 4, 8, 2)
+    w, slot_of, y, dout = _fuzz(76, 400, 2048, k, 8, 2)
     dy, dw = m.moe_combine_backward(bf16_dev(dout), None, torch.from_numpy(slot_of).cuda(),
                                     torch.from_numpy(w.topk_w).cuda())
     assert dw is None
     assert np.array_equal(bits(dy), oracle.combine_backward(dout, None, slot_of, w.topk_w)[0])
+
+
+def test_combine_backward_dw_is_deterministic():
+    # dw's summation order is fixed (tokens split between two CTAs get exactly
+    # two additions onto zero, whose order cannot change the result)
+    m = cl()
+    w, slot_of, y, dout = _named("dsv3_decode")
+    args = (bf16_dev(dout), bf16_dev(y), torch.from_numpy(slot_of).cuda(),
+            torch.from_numpy(w.topk_w).cuda())
+    runs = [m.moe_combine_backward(*args)[1].cpu().numpy().view(np.uint32) for _ in range(3)]
+    assert all(np.array_equal(runs[0], r) for r in runs[1:])
 
 
 @pytest.mark.parametrize("name", ["tiny", "dsv3_decode", "glm45_air", "mixtral"])
@@ -97,6 +113,18 @@ def test_dispatch_backward_fuzz(case):
     w, slot_of, y, _ = _fuzz(*case)
     dx = m.moe_dispatch_backward(bf16_dev(y), torch.from_numpy(slot_of).cuda())
     assert np.array_equal(bits(dx), oracle.dispatch_backward(y, slot_of, "bf16"))
+
+
+def test_combine_backward_bad_slot_reported_k8():
+    m = cl()
+    err = m.new_error_word()
+    T, k, H = 300, 8, 512
+    so = torch.arange(T * k, dtype=torch.int32, device="cuda").view(T, k)
+    so[123, 5] = T * k + 7
+    d = torch.ones((T, H), dtype=torch.bfloat16, device="cuda")
+    yv = torch.ones((T * k, H), dtype=torch.bfloat16, device="cuda")
+    m.moe_combine_backward(d, yv, so, torch.ones((T, k), device="cuda"), err_word=err)
+    assert m.moe_read_error(err) == m.MOE_ERRBIT_BAD_INDEX
 
 
 def test_backward_bad_slot_reported():
