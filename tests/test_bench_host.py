@@ -59,6 +59,26 @@ def test_byte_model_dsv3_decode():
     assert fp8 == 2 * 8192 * 7168 + 4 * 65536 + 65536 * 7168 + 4 * 65536 * 56
 
 
+def test_byte_model_backward_and_coalesced():
+    T, H, k, E, R = 1024, 7168, 8, 256, 32
+    N = T * k
+    # dy is a k-row scatter of dout; dw reads the same k rows of y
+    assert bench.kernel_bytes("combine_backward", T, H, k, E, R) == \
+        2 * T * H + 2 * N * H + 2 * N * H + 12 * N
+    # dx is the unit-weight combine: no weights read
+    assert bench.kernel_bytes("dispatch_backward", T, H, k, E, R) == \
+        bench.kernel_bytes("combine", T, H, k, E, R) - 4 * N
+    assert bench.kernel_bytes("layout_dispatch", T, H, k, E, R) == \
+        bench.kernel_bytes("layout_assign", T, H, k, E, R) + \
+        bench.kernel_bytes("dispatch_bf16", T, H, k, E, R)
+    Nc = 7464
+    assert bench.coalesced_bytes("dispatch_coalesced", T, H, k, Nc) == 2 * T * H + 4 * N + 2 * Nc * H
+    # with one row per slot, the coalesced combine moves the plain combine's
+    # bytes plus the rows it pre-reduces and the coalesced row map
+    assert bench.coalesced_bytes("combine_coalesced", T, H, k, N) == \
+        bench.kernel_bytes("combine", T, H, k, E, R) + 2 * N * H + 4 * N
+
+
 def test_reference_arm_prints_one_json_line():
     buf = io.StringIO()
     with redirect_stdout(buf):
