@@ -210,7 +210,9 @@ MOE_API moe_status moe_combine(int T, int H, int k, const void *y, const int32_t
  *                      in fp32 in a fixed order (deterministic; within
  *                      (H-1) * 2^-24 * sum|y * dout| of the exact value)
  *
- * 1 <= k <= 32; H % 8 == 0.
+ * 1 <= k <= 32; H % 8 == 0.  For 5 <= k <= 8 the call first zero-fills dw on
+ * the stream (an asynchronous memset, then the kernel adds at most two partial
+ * sums per element, whose order cannot change the result).
  */
 MOE_API moe_status moe_combine_backward(int T, int H, int k, const void *dout, const void *y,
                                 const int32_t *slot_of, const float *topk_w, void *dy,
