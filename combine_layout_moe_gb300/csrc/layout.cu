@@ -43,7 +43,10 @@ constexpr int LAYOUT_WARPS = LAYOUT_THREADS / 32;
 constexpr int LAYOUT_TARGET_TILE = MOE_LAYOUT_TARGET_TILE;  // pairs per CTA while tiles are few
 constexpr int LAYOUT_MAX_TILES = 128;     // bounds the tile-count table each CTA reads
 constexpr int LAYOUT_BATCH = 8;           // expert ids loaded ahead per lane
-constexpr int TABLE_UNROLL = 8;           // independent table loads in flight per thread
+#ifndef MOE_LAYOUT_TABLE_UNROLL
+#define MOE_LAYOUT_TABLE_UNROLL 8
+#endif
+constexpr int TABLE_UNROLL = MOE_LAYOUT_TABLE_UNROLL;  // independent table loads in flight per thread
 constexpr size_t LAYOUT_BARRIER_BYTES = 256;  // workspace head: grid-barrier count and generation
 constexpr int CLUSTER_MAX_TILES = 8;          // portable thread-block cluster size
 
@@ -235,11 +238,15 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
             report(err_word, MOE_ERRBIT_TIMEOUT);
         for (int e = tid; e < E; e += LAYOUT_THREADS) {
             const uint32_t la = smem_addr(tsum + e);
+            int32_t v[CLUSTER_MAX_TILES];
+#pragma unroll
+            for (int b = 0; b < CLUSTER_MAX_TILES; ++b)  // all remote loads in flight at once
+                v[b] = b < nread ? ld_dsmem_s32(la, (uint32_t)b) : 0;
             int32_t before = 0, total = 0;
-            for (int b = 0; b < nread; ++b) {
-                const int32_t v = ld_dsmem_s32(la, (uint32_t)b);
-                total += v;
-                before += b < (int)blockIdx.x ? v : 0;
+#pragma unroll
+            for (int b = 0; b < CLUSTER_MAX_TILES; ++b) {
+                total += v[b];
+                before += b < (int)blockIdx.x ? v[b] : 0;
             }
             offs[e] = total;
             pre[e] = before;
