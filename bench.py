@@ -252,6 +252,53 @@ def oracle_step(w, y_np, fp8: bool):
     oracle.combine(y_np, slot_of, w.topk_w, "bf16")
 
 
+def host_info():
+    """The host's logical CPU count and CPU model (from /proc/cpuinfo)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            fields = {}
+            for ln in f:
+                if ":" in ln:
+                    k_, v_ = (t.strip() for t in ln.split(":", 1))
+                    fields.setdefault(k_, v_)
+        model = fields.get("model name") or fields.get("Model Name")
+        if model is None and "CPU part" in fields:
+            model = f"implementer {fields.get('CPU implementer')} part {fields['CPU part']}"
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu": model}
+
+
+def cpu_baseline_table(args):
+    """The oracle's time per operation on every workload, on one host core:
+    the median of 3 runs of each (layout, dispatch of the workload's payload,
+    combine).  One JSON line per (workload, operation)."""
+    import oracle
+    from workloads.gen import make_workload, expert_output, CONFIGS, CONFIG_ORDER
+    host = host_info()
+    for name in CONFIG_ORDER:
+        w = make_workload(name)
+        y = expert_output(w.N, w.H, seed=w.seed)
+        fp8 = CONFIGS[name]["payload"] == "fp8"
+        _, _, _, slot_of, _ = oracle.layout(w.topk_idx, w.E, w.R)
+        ops = [("layout", lambda: oracle.layout(w.topk_idx, w.E, w.R)),
+               ("dispatch_fp8" if fp8 else "dispatch_bf16",
+                (lambda: oracle.dispatch_quant(w.x, slot_of)) if fp8
+                else (lambda: oracle.dispatch(w.x, slot_of))),
+               ("combine", lambda: oracle.combine(y, slot_of, w.topk_w, "bf16"))]
+        for op, fn in ops:
+            ts = []
+            for _ in range(3):
+                t0 = time.perf_counter()
+                fn()
+                ts.append(time.perf_counter() - t0)
+            med = statistics.median(ts)
+            print(json.dumps({"workload": name, "op": op, "oracle_median_ms": round(1e3 * med, 3),
+                              "tokens_per_s": round(w.T / med, 1), "cores": 1,
+                              "host": host}), flush=True)
+
+
 def cpu_baseline(name: str, budget_s: float = 12.0):
     """The oracle on the host, single-threaded, over whole steps of the workload
     until `budget_s` of CPU work (at least one step)."""
@@ -268,6 +315,7 @@ def cpu_baseline(name: str, budget_s: float = 12.0):
         if el >= budget_s:
             break
     return {"value": steps * w.T / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "host": host_info(),
             "sample": f"{steps} whole {name} steps (T={w.T}: layout + "
                       f"{'fp8 ' if fp8 else ''}dispatch + combine), single-threaded C, "
                       f"{el:.1f} s"}
@@ -301,6 +349,7 @@ def run_reference(args):
         "config": {"workload": f"{name} T={c['T']} H={c['H']} k={c['k']} E={c['E']} R={c['R']}",
                    "sample_tokens_per_step": Ts},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "host": host_info(),
                          "sample": f"each step: the {name} recipe at T={Ts} tokens "
                                    f"(layout + {'fp8 ' if fp8 else ''}dispatch + combine)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -804,10 +853,15 @@ def main(argv=None):
                    help="with --table: the single-kernel Data-as-Flag variant per readiness "
                         "mode and granularity, against separate launches")
     p.add_argument("--table-reps", type=int, default=50)
+    p.add_argument("--cpu-baseline-table", action="store_true",
+                   help="the oracle's time per operation on every workload, one host core "
+                        "(median of 3); no GPU")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
-    if args.table or args.table_all or args.table_flagged:
+    if args.cpu_baseline_table:
+        cpu_baseline_table(args)
+    elif args.table or args.table_all or args.table_flagged:
         run_table(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -95,3 +95,9 @@ def test_reference_arm_prints_one_json_line():
 def test_warmup_below_three_rejected():
     with pytest.raises(SystemExit):
         bench.main(["--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "2"])
+
+
+def test_host_info_reports_core_count():
+    h = bench.host_info()
+    assert h["nproc"] == os.cpu_count() and h["nproc"] >= 1
+    assert h["cpu"] is None or isinstance(h["cpu"], str)
