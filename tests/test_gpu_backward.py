@@ -65,7 +65,10 @@ def test_combine_backward_matches_oracle(name):
 # per row as well as many
 FUZZ = [(71, 1, 8, 1, 1, 1), (72, 33, 264, 3, 5, 5), (73, 100, 7176, 8, 16, 4),
         (74, 17, 1024, 16, 20, 4), (75, 9, 512, 32, 40, 8), (78, 777, 1000, 5, 10, 5),
-        (79, 7, 4096, 6, 12, 3), (80, 3001, 136, 7, 7, 7), (81, 1, 16384, 8, 8, 2)]
+        (79, 7, 4096, 6, 12, 3), (80, 3001, 136, 7, 7, 7), (81, 1, 16384, 8, 8, 2),
+        # H = 262144: the pipeline's ring and stages exceed shared memory, so
+        # the CTA-per-token kernel takes k = 8
+        (82, 2, 262144, 8, 8, 2)]
 
 
 @pytest.mark.parametrize("case", FUZZ, ids=[f"T{c[1]}_H{c[2]}_k{c[3]}" for c in FUZZ])
