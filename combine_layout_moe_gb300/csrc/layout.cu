@@ -13,8 +13,8 @@
 //      expert ids stay in registers); the CTA writes the row sums to its row of
 //      the tile-count table.
 //   2. Grid barrier (arrival count and generation in the workspace; bounded).
-//      With at most CLUSTER_MAX_TILES tiles the grid is one thread-block
-//      cluster instead: each CTA keeps its row in shared memory, a hardware
+//      With at most CLUSTER_MAX_TILES (16) tiles the grid is one thread-block
+//      cluster instead (sizes above 8 only where the GPU can place one): each CTA keeps its row in shared memory, a hardware
 //      cluster barrier replaces the grid barrier, and step 3 reads the other
 //      CTAs' rows through distributed shared memory (no table in global
 //      memory, no atomics, no polling).
@@ -48,7 +48,8 @@ constexpr int LAYOUT_BATCH = 8;           // expert ids loaded ahead per lane
 #endif
 constexpr int TABLE_UNROLL = MOE_LAYOUT_TABLE_UNROLL;  // independent table loads in flight per thread
 constexpr size_t LAYOUT_BARRIER_BYTES = 256;  // workspace head: grid-barrier count and generation
-constexpr int CLUSTER_MAX_TILES = 8;          // portable thread-block cluster size
+constexpr int CLUSTER_MAX_TILES = 16;         // largest cluster (non-portable beyond 8)
+constexpr int CLUSTER_PORTABLE = 8;           // cluster sizes every sm_90+ GPU accepts
 
 // Thread-block cluster barrier, split into its arrive (release) and wait
 // (acquire) halves; every thread of every CTA of the cluster takes part.
@@ -238,15 +239,17 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
             report(err_word, MOE_ERRBIT_TIMEOUT);
         for (int e = tid; e < E; e += LAYOUT_THREADS) {
             const uint32_t la = smem_addr(tsum + e);
-            int32_t v[CLUSTER_MAX_TILES];
-#pragma unroll
-            for (int b = 0; b < CLUSTER_MAX_TILES; ++b)  // all remote loads in flight at once
-                v[b] = b < nread ? ld_dsmem_s32(la, (uint32_t)b) : 0;
             int32_t before = 0, total = 0;
+            for (int b0 = 0; b0 < nread; b0 += CLUSTER_PORTABLE) {
+                int32_t v[CLUSTER_PORTABLE];
 #pragma unroll
-            for (int b = 0; b < CLUSTER_MAX_TILES; ++b) {
-                total += v[b];
-                before += b < (int)blockIdx.x ? v[b] : 0;
+                for (int q = 0; q < CLUSTER_PORTABLE; ++q)  // eight remote loads in flight at once
+                    v[q] = b0 + q < nread ? ld_dsmem_s32(la, (uint32_t)(b0 + q)) : 0;
+#pragma unroll
+                for (int q = 0; q < CLUSTER_PORTABLE; ++q) {
+                    total += v[q];
+                    before += b0 + q < (int)blockIdx.x ? v[q] : 0;
+                }
             }
             offs[e] = total;
             pre[e] = before;
@@ -472,14 +475,31 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, 
         attr[0].val.clusterDim.x = (unsigned)p.tiles;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        e = launch(1, 2);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            e = launch(1, 1);  // without the programmatic attribute
+        bool fits = true;
+        if (p.tiles > CLUSTER_PORTABLE) {
+            // a non-portable size: allowed explicitly, and used only if the
+            // GPU can place one such cluster of these CTAs
+            int nclusters = 0;
+            cfg.numAttrs = 1;
+            fits = cudaFuncSetAttribute(layout_kernel<NBITS, COAL>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                        1) == cudaSuccess &&
+                   cudaOccupancyMaxActiveClusters(&nclusters, layout_kernel<NBITS, COAL>,
+                                                  &cfg) == cudaSuccess &&
+                   nclusters >= 1;
+            if (!fits)
+                (void)cudaGetLastError();
         }
-        if (e == cudaSuccess)
-            return e;
-        (void)cudaGetLastError();  // no cluster of this size: the cooperative form below
+        if (fits) {
+            e = launch(1, 2);
+            if (e != cudaSuccess) {
+                (void)cudaGetLastError();
+                e = launch(1, 1);  // without the programmatic attribute
+            }
+            if (e == cudaSuccess)
+                return e;
+            (void)cudaGetLastError();  // no cluster of this size: the cooperative form below
+        }
     }
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;

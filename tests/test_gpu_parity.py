@@ -78,9 +78,12 @@ FUZZ = [  # (seed, T, k, E, R)
     (6, 257, 4, 256, 32), (7, 4097, 3, 5, 5), (8, 5000, 8, 1024, 8), (9, 12345, 6, 64, 16),
     (10, 70000, 2, 2, 2), (11, 100000, 8, 128, 16), (12, 300000, 8, 256, 32),
     (13, 2049, 1, 3, 1), (14, 511, 16, 40, 10), (15, 40, 33, 9, 3),
-    # around the one-cluster form (at most 8 tiles of ~1024 pairs): 8000 pairs
-    # with the largest expert count, 8192 pairs (8 tiles), 8193 pairs (9 tiles)
+    # around the one-cluster form (at most 16 tiles of ~1024 pairs; above 8 a
+    # non-portable cluster): 8000 pairs with the largest expert count, 8192
+    # pairs (8 tiles), 8193 (9), 12000 (12), 16384 (16) and 16385 (17 tiles:
+    # the grid-barrier form)
     (16, 1000, 8, 1024, 8), (17, 4096, 2, 32, 4), (18, 8193, 1, 64, 4),
+    (19, 1500, 8, 1024, 32), (20, 2048, 8, 256, 32), (21, 16385, 1, 16, 4),
 ]
 
 
@@ -115,7 +118,7 @@ def test_layout_empty():
     assert lay.rank_offsets.cpu().tolist() == [0] * 3
 
 
-@pytest.mark.parametrize("T", [64, 2048, 20000])   # one tile, one cluster, the grid barrier
+@pytest.mark.parametrize("T", [64, 2048, 6000, 20000])  # one tile, clusters of 4 and 12, the grid barrier
 def test_layout_bad_index_reported(T):
     m = cl()
     err = m.new_error_word()
