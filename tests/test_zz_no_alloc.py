@@ -34,8 +34,10 @@ def _noalloc_via_abi(m, idx, E, R, out, err):
 
 def test_noalloc_layout_matches_moe_layout_on_consecutive_calls():
     import combine_layout_moe_gb300 as m
+    # the grid-barrier form (which uses the fixed array), clusters of 8 and 16
+    # CTAs (which do not), then the grid-barrier form again
     cases = [make_workload("glm45_air"), make_workload("dsv3_decode"),
-             random_case(77, 3000, 8, 6, 40, 8)]
+             random_case(78, 2048, 8, 8, 256, 32), random_case(77, 3000, 8, 6, 40, 8)]
     err = m.new_error_word()
     for w in cases:                                   # two and more calls in a row
         idx = torch.from_numpy(w.topk_idx).cuda()
