@@ -104,3 +104,22 @@ def test_empty_tokens():
     out = oracle.combine(np.zeros((0, 16), np.uint16), np.zeros((0, 2), np.int32),
                          np.zeros((0, 2), np.float32))
     assert out.shape == (0, 16)
+
+
+def test_each_slot_is_one_fused_multiply_add():
+    """k = 2, y = (1 + 2^-7, 1 + 2^-7) (exact bf16), w = (-1, 1 + 2^-23) (exact
+    fp32).  The exact value of w1*y1 + w0*y0 is 2^-23 (1 + 2^-7) = 2^-23 +
+    2^-30, which fp32 holds.  One fused multiply-add per slot keeps it: the
+    running sum after slot 0 is -(1 + 2^-7) exactly, and slot 1 rounds the
+    exact w1*y1 + acc once.  Rounding the product first (to 1 + 2^-7 + 2^-23,
+    the 2^-30 lies below half an ulp at 1) and then adding would give 2^-23."""
+    y = np.full((2, 8), 0x3F81, np.uint16)          # 1.0078125 = 1 + 2^-7
+    slot_of = np.array([[0, 1]], np.int32)
+    wt = np.array([[-1.0, 1.0 + 2.0 ** -23]], np.float32)
+    assert float(wt[0, 1]) == 1.0 + 2.0 ** -23
+    out = oracle.combine(y, slot_of, wt, "f32")
+    assert np.all(out == np.float32(2.0 ** -23 + 2.0 ** -30))
+    # one rounding to bf16: 2^-23 (1 + 2^-7) has 8 significant bits, so it is
+    # exact in bf16: sign 0, biased exponent 127 - 23 = 104, fraction 0000001
+    outb = oracle.combine(y, slot_of, wt, "bf16")
+    assert np.all(outb == (104 << 7) | 1)

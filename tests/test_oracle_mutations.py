@@ -35,6 +35,8 @@ MUTANTS = {
                       "float v = bf16_to_f32(y[(int64_t)slot_of[(int64_t)t * k] * H + h]);"),
     # combine: weight and value of neighbouring slots swapped
     "combine_weight": ("acc = fmaf(topk_w[i], v, acc);", "acc = fmaf(topk_w[(int64_t)t * k + (j + 1) % k], v, acc);"),
+    # combine: product rounded before the add (two roundings per slot, not one)
+    "combine_unfused": ("acc = fmaf(topk_w[i], v, acc);", "acc = acc + topk_w[i] * v;"),
     # backward: dy scaled by the weight of the wrong slot
     "dy_weight": ("const float w = topk_w[i];\n            double acc = 0.0, mag = 0.0;",
                   "const float w = topk_w[(int64_t)t * k];\n            double acc = 0.0, mag = 0.0;"),
@@ -67,6 +69,7 @@ def _pins():
              lambda: td.test_quant_block_invariants(("fuzz", 0)),
              lambda: td.test_dispatch_rows_equal_source_token(("fuzz", 0)),
              tc.test_one_hot_weights_select_one_slot, tc.test_weights_are_not_renormalised,
+             tc.test_each_slot_is_one_fused_multiply_add,
              lambda: tc.test_bf16_output_is_rounded_fp32_output("fuzz0", None),
              tb.test_random_and_special_values_match_torch,
              lambda: tbw.test_combine_backward_matches_autograd(tbw.CASES[1]),
