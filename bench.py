@@ -1,21 +1,29 @@
 """Benchmark: MoE expert-parallel dispatch + combine on one GB300 (or N replicas).
 
-One step = the whole hot path over one batch: layout (count kernel, scan+assign
-kernel) -> dispatch (bf16 row scatter, or the fused FP8 variant for FP8
-workloads) -> combine (router-weighted fp32 gather-reduce, bf16 out) of
-synthetic expert outputs.  Default workload: DeepSeek-V3-style decode batch,
-T=1024, H=7168, top-8 of E=256 experts on R=32 virtual ranks.
+One step = the whole hot path over one batch: layout (count, scan, slot map)
+-> dispatch (bf16 row scatter, or the fused FP8 variant for FP8 workloads) ->
+combine (router-weighted fp32 gather-reduce, bf16 out) of synthetic expert
+outputs.  The headline workload is the largest of the target's single-GPU
+workloads: Mixtral-style, T=65536, H=4096, top-2 of E=8 experts on R=8
+virtual ranks, one hot expert.  The line then carries a `per_config` block:
+the DeepSeek-V3-style decode (T=1024, H=7168, top-8 of 256, R=32) and prefill
+(T=8192, FP8 dispatch) workloads, the GLM-4.5-Air-style workload (T=16384,
+H=4096, top-8 of 128, R=16) and the headline's own figures, each through the
+same timed loop, with its dispatch and combine times, algorithmic bytes and
+fraction of the measured HBM peak, and the oracle's time per operation on one
+host core.
 
 Timing: W untimed warm-up steps, then exactly K timed steps between a barrier
 and a device synchronisation.  Every step flushes L2 twice, outside the CUDA
-events that bracket each kernel on the launching stream: a 2xL2 buffer is
+events that bracket each segment on the launching stream: a 2xL2 buffer is
 written before layout+dispatch (dispatch then pays for evicting dirty lines,
 as its own writes would), and a 4xL2 buffer is read before combine
 (combine starts from a cold, clean L2 and is not charged for dispatch's
 write-backs).  value = tokens per second over all ranks (weak scaling: each
-rank runs its own replica).  `e2e` repeats the
-step through the public API with each step's inputs copied from pinned host
-memory and its combined output copied back, pipelined over three streams.
+rank runs its own replica).  SM clocks and clock-event reasons are sampled
+through NVML about every millisecond inside each timed region.  `e2e` repeats
+the step through the public API with each step's inputs copied from pinned
+host memory and its combined output copied back, pipelined over three streams.
 
 --variant coalesced times the rank-coalesced path instead: layout ->
 coalesced layout -> coalesced dispatch (one row per token and destination
@@ -48,7 +56,9 @@ import numpy as np  # noqa: E402
 
 METRIC = "dispatch+combine tokens/s"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "dsv3_decode"
+DEFAULT_WORKLOAD = "mixtral"
+# the workloads the target names (configs 1-4), measured after the headline
+PER_CONFIG = "dsv3_decode,dsv3_prefill,glm45_air,mixtral"
 
 
 # ------------------------------------------------------------------ bytes
@@ -223,13 +233,15 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if that kernel's
-    source is unchanged since the counters were taken; else None."""
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summaries, if that kernel's source is unchanged since the counters were
+    taken; else None.  Entries are keyed "kernel@workload" (a capture of a
+    smaller case of the same workload states how it was scaled)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(kernel)
+            rec = json.load(f).get(f"{kernel}@{workload}")
         src = os.path.join(ROOT, rec["source"])
         with open(src, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()
@@ -242,13 +254,14 @@ def recorded_traffic(kernel: str):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_step(w, y_np, fp8: bool):
+def oracle_step(w, y_np, fp8: bool, x_np=None):
     import oracle
+    x_np = w.x if x_np is None else x_np
     counts, offs, roffs, slot_of, src_of = oracle.layout(w.topk_idx, w.E, w.R)
     if fp8:
-        oracle.dispatch_quant(w.x, slot_of)
+        oracle.dispatch_quant(x_np, slot_of)
     else:
-        oracle.dispatch(w.x, slot_of)
+        oracle.dispatch(x_np, slot_of)
     oracle.combine(y_np, slot_of, w.topk_w, "bf16")
 
 
@@ -299,17 +312,19 @@ def cpu_baseline_table(args):
                               "host": host}), flush=True)
 
 
-def cpu_baseline(name: str, budget_s: float = 12.0):
+def cpu_baseline(name: str, budget_s: float = 12.0, w=None, x_np=None, y_np=None):
     """The oracle on the host, single-threaded, over whole steps of the workload
-    until `budget_s` of CPU work (at least one step)."""
+    until `budget_s` of CPU work (at least one step).  `w`, `x_np`, `y_np`: the
+    workload and the bit patterns of the inputs the GPU step used (drawn here
+    when not given)."""
     from workloads.gen import make_workload, expert_output, CONFIGS
-    w = make_workload(name)
-    y = expert_output(w.N, w.H, seed=w.seed)
+    w = make_workload(name) if w is None else w
+    y = expert_output(w.N, w.H, seed=w.seed) if y_np is None else y_np
+    x = w.x if x_np is None else x_np
     fp8 = CONFIGS[name]["payload"] == "fp8"
-    _ = w.x
     steps, t0 = 0, time.perf_counter()
     while True:
-        oracle_step(w, y, fp8)
+        oracle_step(w, y, fp8, x)
         steps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -359,6 +374,375 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU arm
 
+class NvmlClocks:
+    """Samples the SM clock and the clock-event reasons of one GPU through NVML
+    (read-only queries, via ctypes on the driver's libnvidia-ml) on a thread,
+    every ~1 ms while a window is open, so that a timed region of a few
+    milliseconds still gets samples.  Unavailable NVML leaves no samples."""
+    NVML_CLOCK_SM = 1
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.ok = False
+        self.samples = []      # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self._stop = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+            self._lib, self._h, self._ct = lib, h, ctypes
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _one(self):
+        ct = self._ct
+        c = ct.c_uint()
+        r = ct.c_ulonglong(0)
+        if self._lib.nvmlDeviceGetClockInfo(self._h, self.NVML_CLOCK_SM, ct.byref(c)) != 0:
+            return None
+        if self._reasons is not None:
+            self._reasons(self._h, ct.byref(r))
+        return float(c.value), int(r.value)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def _run(self):
+        while not self._stop.is_set():
+            s = self._one()
+            if s is not None:
+                self.samples.append(s)
+            time.sleep(0.001)
+
+    def __exit__(self, *a):
+        if self._stop is not None:
+            self._stop.set()
+            self._t.join(timeout=2)
+            s = self._one()      # and one at the end of the window
+            if s is not None:
+                self.samples.append(s)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml"}
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_min_mhz": min(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASON_BITS.items() if bits & b),
+                "samples": len(self.samples), "source": "nvml, ~1 ms, inside the timed region"}
+
+
+def _ms_list(evs, a, b):
+    return [e[a].elapsed_time(e[b]) for e in evs]
+
+
+class StepBench:
+    """Buffers and launch arguments of one workload's step, all resident in
+    HBM, and the timed loop over it.
+
+    A step is layout -> dispatch -> combine.  The front segment (A1-A4, or
+    A1-A3 + A5 for an FP8 workload) is timed by one event pair; so is the
+    combine.  Before the front, a 2xL2 buffer is written (the dispatch pays
+    for evicting dirty lines, as its own writes eventually would); before the
+    combine, a 4xL2 buffer is read (the combine starts from a cold, clean L2
+    and is not charged for the dispatch's write-backs).  Both flushes sit
+    outside the events."""
+
+    def __init__(self, name, dev, seed, variant, m, keep_host=False):
+        import torch
+        import ctypes
+        from workloads.gen import make_workload, CONFIGS, device_inputs
+        self.name, self.dev, self.m = name, dev, m
+        self.coal = variant == "coalesced"
+        self.fp8 = CONFIGS[name]["payload"] == "fp8"
+        w = make_workload(name, seed=seed)
+        self.w = w
+        T, H, k, E, R, N = w.T, w.H, w.k, w.E, w.R, w.N
+        self.T, self.H, self.k, self.E, self.R, self.N = T, H, k, E, R, N
+        self.x, self.y = device_inputs(w, dev)
+        self.idx = torch.from_numpy(w.topk_idx).to(dev)
+        self.wt = torch.from_numpy(w.topk_w).to(dev)
+        self.err = m.new_error_word(dev)
+        self.ws = m.new_workspace(m.moe_layout_workspace_bytes(T, k, E), dev)
+        lay = m.Layout(torch.empty(E, dtype=torch.int32, device=dev),
+                       torch.empty(E + 1, dtype=torch.int32, device=dev),
+                       torch.empty(R + 1, dtype=torch.int32, device=dev),
+                       torch.empty((T, k), dtype=torch.int32, device=dev),
+                       torch.empty(T * k, dtype=torch.int32, device=dev))
+        self.lay = lay
+        rows = T * min(k, R)   # coalesced rows: at most one per token and rank
+        self.rows = rows
+        nrecv = rows if self.coal else N
+        self.recv = self.recv_q = self.recv_s = None
+        if self.fp8:
+            self.recv_q = torch.empty((nrecv, H), dtype=torch.uint8, device=dev)
+            self.recv_s = torch.empty((nrecv, H // 128), dtype=torch.float32, device=dev)
+        else:
+            self.recv = torch.empty((nrecv, H), dtype=torch.bfloat16, device=dev)
+        if self.coal:
+            self.partial = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+            self.wsc = m.new_workspace(m.moe_layout_workspace_bytes(T, k, R), dev)
+            self.co = m.CoalescedLayout(torch.empty(R, dtype=torch.int32, device=dev),
+                                        torch.empty(R + 1, dtype=torch.int32, device=dev),
+                                        torch.empty((T, k), dtype=torch.int32, device=dev),
+                                        torch.empty(T * k, dtype=torch.int32, device=dev),
+                                        torch.empty(T * k, dtype=torch.int32, device=dev))
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+        # Reading 2xL2 once leaves some of the dispatch's dirty lines resident
+        # on GB300 (combine then pays ~1.6 us of their write-back); one read of
+        # 4xL2 evicts them all.
+        self.flush_r = torch.zeros(max(4 * l2, 512 << 20), dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+        # The step calls the C ABI directly with pre-marshalled arguments, so
+        # host time between launches stays far below the GPU time of a step.
+        L = m._lib
+        self.L = L
+        cs = ctypes.c_void_p(self.stream.cuda_stream)
+        P = lambda t: t.data_ptr()  # noqa: E731
+        self.lay_args = (T, k, E, R, P(self.idx), P(lay.expert_counts), P(lay.expert_offsets),
+                         P(lay.rank_offsets), P(lay.slot_of), P(lay.src_of), P(self.ws),
+                         self.ws.numel(), P(self.err), cs)
+        x, y, err, wt = self.x, self.y, self.err, self.wt
+        if self.fp8 and self.coal:
+            co = self.co
+            self.disp = (L.moe_dispatch_quant_coalesced,
+                         (T, H, k, P(x), P(co.crow), rows, P(self.recv_q), P(self.recv_s),
+                          P(err), cs))
+        elif self.fp8:
+            self.disp = (L.moe_dispatch_quant, (T, H, k, P(x), P(lay.slot_of), P(self.recv_q),
+                                                P(self.recv_s), P(err), cs))
+        elif self.coal:
+            self.disp = (L.moe_dispatch_coalesced, (T, H, k, P(x), P(self.co.crow), rows,
+                                                    P(self.recv), P(err), cs))
+        else:
+            self.disp = (L.moe_dispatch, (T, H, k, P(x), P(lay.slot_of), P(self.recv), P(err),
+                                          cs))
+        if self.coal:
+            co = self.co
+            self.coal_args = (T, k, E, R, P(self.idx), P(lay.slot_of), P(co.rank_counts_c),
+                              P(co.rank_offsets_c), P(co.crow), P(co.src_pair_c), P(co.expand),
+                              P(self.wsc), self.wsc.numel(), P(err), cs)
+            self.comb = (L.moe_combine_coalesced, (T, H, k, P(y), P(lay.slot_of), P(wt),
+                                                   P(co.crow), rows, P(self.partial), P(self.out),
+                                                   m.MOE_OUT_BF16, P(err), cs))
+        else:
+            self.comb = (L.moe_combine, (T, H, k, P(y), P(lay.slot_of), P(wt), P(self.out),
+                                         m.MOE_OUT_BF16, P(err), cs))
+        # layout then dispatch as one call where the library offers it (bf16):
+        # the dispatch's first loads of x overlap the layout
+        self.fused_front = not self.fp8 and not self.coal
+        self.front_args = (T, H, k, E, R, P(self.idx), P(x), P(lay.expert_counts),
+                           P(lay.expert_offsets), P(lay.rank_offsets), P(lay.slot_of),
+                           P(lay.src_of), P(self.recv) if self.fused_front else None, P(self.ws),
+                           self.ws.numel(), P(err), cs)
+        self.d_name = (("dispatch_fp8_coalesced" if self.fp8 else "dispatch_coalesced")
+                       if self.coal else ("dispatch_fp8" if self.fp8 else "dispatch_bf16"))
+        self.c_name = "combine_coalesced" if self.coal else "combine"
+
+    # -- launches
+    def _call(self, fn, a):
+        st = fn(*a)
+        if st != self.m.MOE_OK:
+            raise self.m.MoeError(st, fn.__name__)
+
+    def layout_only(self):
+        self._call(self.L.moe_layout, self.lay_args)
+        if self.coal:
+            self._call(self.L.moe_layout_coalesced, self.coal_args)
+
+    def dispatch_only(self):
+        self._call(*self.disp)
+
+    def front(self):
+        if self.fused_front:
+            self._call(self.L.moe_layout_dispatch, self.front_args)
+        else:
+            self.layout_only()
+            self.dispatch_only()
+
+    def combine_only(self):
+        self._call(*self.comb)
+
+    def dirty_flush(self):
+        self.flush.fill_(0)
+
+    def clean_flush(self):
+        import torch
+        self.flush_r.view(torch.int64).sum()
+
+    def launches_per_step(self):
+        # layout, dispatch, combine; the coalesced step adds the coalesced
+        # layout (a second launch when k does not divide 32)
+        if self.coal:
+            return 4 if 32 % self.k == 0 else 5
+        return 3
+
+    def step(self, ev=None):
+        st = self.stream
+        self.dirty_flush()
+        if ev:
+            ev[0].record(st)
+        self.front()
+        if ev:
+            ev[1].record(st)
+        self.clean_flush()
+        if ev:
+            ev[2].record(st)
+        self.combine_only()
+        if ev:
+            ev[3].record(st)
+
+    def check_errors(self, where):
+        bits = self.m.moe_read_error(self.err)
+        if bits:
+            raise RuntimeError(f"device error bits {bits:#x} {where} ({self.name})")
+
+    def timed(self, steps, warmup, clocks_uuid=None):
+        """W warm-up steps, then exactly `steps` timed steps between a barrier
+        and a device synchronisation; then a breakdown pass (an event pair
+        around the layout and around the dispatch, outside the timed steps)."""
+        import torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        self.check_errors("during warm-up")
+        self.Nc = int(self.co.rank_offsets_c[self.R].item()) if self.coal else self.N
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        nv = NvmlClocks(clocks_uuid) if clocks_uuid else None
+        barrier()
+        torch.cuda.synchronize()
+        with (nv if nv is not None else _Null()):
+            t0 = time.perf_counter()
+            for i in range(steps):
+                self.step(ev[i])
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - t0
+        barrier()
+        self.check_errors("in the timed steps")
+        t_front = _ms_list(ev, 0, 1)
+        t_comb = _ms_list(ev, 2, 3)
+        nsplit = max(3, min(steps, 200))
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsplit)]
+        for i in range(nsplit):
+            self.dirty_flush()
+            evs[i][0].record(self.stream)
+            self.layout_only()
+            evs[i][1].record(self.stream)
+            self.dispatch_only()
+            evs[i][2].record(self.stream)
+        torch.cuda.synchronize()
+        self.check_errors("in the breakdown pass")
+        return {"t_front": t_front, "t_comb": t_comb, "t_layout": _ms_list(evs, 0, 1),
+                "t_disp": _ms_list(evs, 1, 2), "wall": wall,
+                "clocks": nv.summary() if nv is not None else None}
+
+    def bytes_of(self, name):
+        T, H, k, E, R = self.T, self.H, self.k, self.E, self.R
+        if self.coal:
+            if name == "front":
+                return (kernel_bytes("layout_assign", T, H, k, E, R) +
+                        coalesced_bytes("layout_coalesced", T, H, k, self.Nc) +
+                        coalesced_bytes(self.d_name, T, H, k, self.Nc))
+            return coalesced_bytes(name, T, H, k, self.Nc)
+        if name == "front":
+            return kernel_bytes("layout_assign", T, H, k, E, R) + kernel_bytes(self.d_name, T, H,
+                                                                               k, E, R)
+        return kernel_bytes(name, T, H, k, E, R)
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def _frac(nbytes, ms, peak):
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    return {"ms": ms, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak}
+
+
+def per_config_entry(b: StepBench, r: dict, peak: float) -> dict:
+    """The in-step figures of one workload: the front segment (the pages'
+    dispatch, A1-A4/A5: layout and dispatch), the dispatch kernel alone (the
+    breakdown pass), and the combine (timed steps), each with its algorithmic
+    bytes and the fraction of the measured HBM peak."""
+    front = statistics.mean(r["t_front"])
+    comb = statistics.mean(r["t_comb"])
+    disp = statistics.mean(r["t_disp"])
+    steps = len(r["t_front"])
+    return {
+        "workload": f"{b.name} T={b.T} H={b.H} k={b.k} E={b.E} R={b.R}",
+        "payload": "fp8-e4m3" if b.fp8 else "bf16",
+        "steps": steps,
+        "tokens_per_s": b.T * steps / (sum(r["t_front"]) + sum(r["t_comb"])) * 1000.0,
+        "ms_per_step": front + comb,
+        "dispatch": dict(_frac(b.bytes_of("front"), front, peak),
+                         what="layout + dispatch in the timed steps (A1-A4 or A1-A3 + A5)",
+                         call="moe_layout_dispatch" if b.fused_front else
+                              f"moe_layout + {b.disp[0].__name__}"),
+        "dispatch_kernel": dict(_frac(b.bytes_of(b.d_name), disp, peak),
+                                what="the dispatch kernel alone, breakdown pass"),
+        "layout_ms": statistics.mean(r["t_layout"]),
+        "combine": dict(_frac(b.bytes_of(b.c_name), comb, peak),
+                        what="combine in the timed steps"),
+    }
+
+
+def oracle_op_times(name, x_bits, y_bits, w, budget_s=1.0):
+    """The oracle's time per operation on the full workload, on one host core:
+    each op once, repeated (median of up to 3) while it stays under
+    `budget_s` in total."""
+    import oracle
+    from workloads.gen import CONFIGS
+    fp8 = CONFIGS[name]["payload"] == "fp8"
+    _, _, _, slot_of, _ = oracle.layout(w.topk_idx, w.E, w.R)
+    ops = [("layout", lambda: oracle.layout(w.topk_idx, w.E, w.R)),
+           ("dispatch_fp8" if fp8 else "dispatch_bf16",
+            (lambda: oracle.dispatch_quant(x_bits, slot_of)) if fp8
+            else (lambda: oracle.dispatch(x_bits, slot_of))),
+           ("combine", lambda: oracle.combine(y_bits, slot_of, w.topk_w, "bf16"))]
+    res = {}
+    for op, fn in ops:
+        ts = []
+        while len(ts) < 3 and (not ts or sum(ts) < budget_s):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        med = statistics.median(ts)
+        res[op] = {"ms": 1e3 * med, "tokens_per_s": w.T / med, "reps": len(ts)}
+    return res
+
+
+def host_bits(t):
+    """uint16 numpy bit patterns of a bf16 device tensor."""
+    import torch
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -370,301 +754,77 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
 
     import combine_layout_moe_gb300 as m
-    from workloads.gen import make_workload, expert_output, CONFIGS
 
     name = args.config
-    c = CONFIGS[name]
-    coal = args.variant == "coalesced"
-    fp8 = c["payload"] == "fp8"
-    w = make_workload(name, seed=args.seed + rank)
-    T, H, k, E, R, N = w.T, w.H, w.k, w.E, w.R, w.N
+    uuid = gpu_smi_id(torch, dev)
+    peak, peak_kind = measured_peak_gbs()
+    b = StepBench(name, dev, args.seed + rank, args.variant, m)
+    T, H, k, E, R, N = b.T, b.H, b.k, b.E, b.R, b.N
+    coal, fp8 = b.coal, b.fp8
 
-    # inputs resident in HBM
-    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
-    idx = torch.from_numpy(w.topk_idx).to(dev)
-    wt = torch.from_numpy(w.topk_w).to(dev)
-    y = torch.from_numpy(expert_output(N, H, seed=w.seed).view(np.int16)).to(dev).view(torch.bfloat16)
-    err = m.new_error_word(dev)
-    ws = m.new_workspace(m.moe_layout_workspace_bytes(T, k, E), dev)
-    lay = m.Layout(torch.empty(E, dtype=torch.int32, device=dev),
-                   torch.empty(E + 1, dtype=torch.int32, device=dev),
-                   torch.empty(R + 1, dtype=torch.int32, device=dev),
-                   torch.empty((T, k), dtype=torch.int32, device=dev),
-                   torch.empty(T * k, dtype=torch.int32, device=dev))
-    rows = T * min(k, R)   # coalesced rows: at most one per token and rank
-    nrecv = rows if coal else N
-    if fp8:
-        recv_q = torch.empty((nrecv, H), dtype=torch.uint8, device=dev)
-        recv_s = torch.empty((nrecv, H // 128), dtype=torch.float32, device=dev)
-    else:
-        recv = torch.empty((nrecv, H), dtype=torch.bfloat16, device=dev)
-    if coal:
-        partial = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
-        wsc = m.new_workspace(m.moe_layout_workspace_bytes(T, k, R), dev)
-        co = m.CoalescedLayout(torch.empty(R, dtype=torch.int32, device=dev),
-                               torch.empty(R + 1, dtype=torch.int32, device=dev),
-                               torch.empty((T, k), dtype=torch.int32, device=dev),
-                               torch.empty(T * k, dtype=torch.int32, device=dev),
-                               torch.empty(T * k, dtype=torch.int32, device=dev))
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    # Reading 2xL2 once leaves some of the dispatch's dirty lines resident on
-    # GB300 (combine then pays ~1.6 us of their write-back); one read of 4xL2
-    # evicts them all (measured: 31.2 -> 29.6 us, the same as after a read-only
-    # history).
-    flush_r = torch.zeros(max(4 * l2, 512 << 20), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    # The step calls the C ABI directly with pre-marshalled arguments, so that
-    # host time between launches stays far below the GPU time of a step.
-    import ctypes
-    L = m._lib
-    cs = ctypes.c_void_p(stream.cuda_stream)
-    P = lambda t: t.data_ptr()  # noqa: E731
-    lay_args = (T, k, E, R, P(idx), P(lay.expert_counts), P(lay.expert_offsets),
-                P(lay.rank_offsets), P(lay.slot_of), P(lay.src_of), P(ws), ws.numel(), P(err), cs)
-    if fp8 and coal:
-        disp_fn, disp_args = L.moe_dispatch_quant_coalesced, (T, H, k, P(x), P(co.crow), rows,
-                                                              P(recv_q), P(recv_s), P(err), cs)
-    elif fp8:
-        disp_fn, disp_args = L.moe_dispatch_quant, (T, H, k, P(x), P(lay.slot_of), P(recv_q),
-                                                    P(recv_s), P(err), cs)
-    elif coal:
-        disp_fn, disp_args = L.moe_dispatch_coalesced, (T, H, k, P(x), P(co.crow), rows, P(recv),
-                                                        P(err), cs)
-    else:
-        disp_fn, disp_args = L.moe_dispatch, (T, H, k, P(x), P(lay.slot_of), P(recv), P(err), cs)
-    if coal:
-        coal_args = (T, k, E, R, P(idx), P(lay.slot_of), P(co.rank_counts_c),
-                     P(co.rank_offsets_c), P(co.crow), P(co.src_pair_c), P(co.expand), P(wsc),
-                     wsc.numel(), P(err), cs)
-        comb_fn, comb_args = L.moe_combine_coalesced, (T, H, k, P(y), P(lay.slot_of), P(wt),
-                                                       P(co.crow), rows, P(partial), P(out),
-                                                       m.MOE_OUT_BF16, P(err), cs)
-    else:
-        comb_fn, comb_args = L.moe_combine, (T, H, k, P(y), P(lay.slot_of), P(wt), P(out),
-                                             m.MOE_OUT_BF16, P(err), cs)
-
-    def call(fn, a):
-        st = fn(*a)
-        if st != m.MOE_OK:
-            raise m.MoeError(st, fn.__name__)
-
-    def layout_only():
-        call(L.moe_layout, lay_args)
-        if coal:
-            call(L.moe_layout_coalesced, coal_args)
-
-    def dispatch_only():
-        call(disp_fn, disp_args)
-
-    # layout then dispatch as one call where the library offers it (bf16): the
-    # dispatch's first loads of x overlap the layout
-    fused_front = not fp8 and not coal
-    front_args = (T, H, k, E, R, P(idx), P(x), P(lay.expert_counts), P(lay.expert_offsets),
-                  P(lay.rank_offsets), P(lay.slot_of), P(lay.src_of),
-                  P(recv) if fused_front else None, P(ws), ws.numel(), P(err), cs)
-
-    def front():
-        if fused_front:
-            call(L.moe_layout_dispatch, front_args)
-        else:
-            layout_only()
-            dispatch_only()
-
-    def combine_only():
-        call(comb_fn, comb_args)
-
-    def dirty_flush():
-        # write 2xL2: the next kernel starts with L2 full of dirty foreign lines
-        # and pays their write-back, as a write-heavy kernel must
-        flush.fill_(0)
-
-    def clean_flush():
-        # then read 4xL2: the next kernel starts with a cold L2 of clean lines,
-        # so a read-heavy kernel is not charged for someone else's write-backs
-        flush_r.view(torch.int64).sum()
-
-    def new_events(n):
-        return [[torch.cuda.Event(enable_timing=True) for _ in range(n)]
-                for _ in range(args.steps)]
-
-    # Timed step: events only at the two segment boundaries, so nothing sits
-    # between dependent kernels (they launch back to back, overlapping their
-    # launch latency through programmatic dependent launch).
-    ev = new_events(4)
-
-    def step(events=None):
-        dirty_flush()
-        if events:
-            events[0].record(stream)
-        front()
-        if events:
-            events[1].record(stream)
-        clean_flush()
-        if events:
-            events[2].record(stream)
-        combine_only()
-        if events:
-            events[3].record(stream)
-
-    # Breakdown pass (not part of the timed steps): an event around each kernel.
-    def step_split(events):
-        dirty_flush()
-        events[0].record(stream)
-        layout_only()
-        events[1].record(stream)
-        dispatch_only()
-        events[2].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    bits = m.moe_read_error(err)
-    if bits:
-        raise RuntimeError(f"device error bits {bits:#x} during warm-up")
-    Nc = int(co.rank_offsets_c[R].item()) if coal else N
-
-    barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(gpu_smi_id(torch, dev)) as clocks:
-        clocks.mark_start()
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            step(ev[i])
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-        clocks.mark_stop()
-    barrier()
-    t_front = [e[0].elapsed_time(e[1]) for e in ev]   # layout + dispatch
-    t_comb = [e[2].elapsed_time(e[3]) for e in ev]
-    t_step = [a + b for a, b in zip(t_front, t_comb)]
+    smi = ClockSampler(uuid).__enter__()   # nvidia-smi, over every timed region
+    smi.mark_start()
+    r = b.timed(args.steps, args.warmup, clocks_uuid=uuid)
+    t_front, t_comb = r["t_front"], r["t_comb"]
+    t_step = [a + c for a, c in zip(t_front, t_comb)]
     total_ms = allreduce_max(sum(t_step))
     ms_per_step = total_ms / args.steps
     value = world * T * args.steps / (total_ms / 1000.0)
 
-    nsplit = max(3, min(args.steps, 200))
-    evs = new_events(3)[:nsplit]
-    for i in range(nsplit):
-        step_split(evs[i])
-    torch.cuda.synchronize()
-    t_layout = [e[0].elapsed_time(e[1]) for e in evs]
-    t_disp = [e[1].elapsed_time(e[2]) for e in evs]
-
     # roofline of the dominant kernel: combine is timed alone inside the timed
     # steps; dispatch (when it dominates) in the breakdown pass.
-    d_name = (("dispatch_fp8_coalesced" if fp8 else "dispatch_coalesced") if coal
-              else ("dispatch_fp8" if fp8 else "dispatch_bf16"))
-    c_name = "combine_coalesced" if coal else "combine"
-    avg_d, avg_c = statistics.mean(t_disp), statistics.mean(t_comb)
+    avg_d, avg_c = statistics.mean(r["t_disp"]), statistics.mean(t_comb)
     if avg_c >= avg_d:
-        dom, dom_ms, source = c_name, avg_c, "timed steps"
+        dom, dom_ms, source = b.c_name, avg_c, "timed steps"
     else:
-        dom, dom_ms, source = d_name, avg_d, "breakdown pass (one event pair per kernel)"
-    dom_bytes = (coalesced_bytes(dom, T, H, k, Nc) if coal else kernel_bytes(dom, T, H, k, E, R))
-    peak, peak_kind = measured_peak_gbs()
+        dom, dom_ms, source = b.d_name, avg_d, "breakdown pass (one event pair per kernel)"
+    dom_bytes = b.bytes_of(dom)
     achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
     kern_name = {"dispatch_bf16": "dispatch_bulk_kernel", "dispatch_fp8": "dispatch_fp8_kernel",
                  "combine": "combine_bulk_kernel",
                  "dispatch_coalesced": "dispatch_bulk_kernel<coalesced>",
                  "dispatch_fp8_coalesced": "dispatch_fp8_kernel<coalesced>",
                  "combine_coalesced": "combine_bulk_kernel<coalesced>"}[dom]
-    tr = None if coal else recorded_traffic(kern_name)
-    traffic = None
-    if tr is not None and tr.get("workload") == name:
-        traffic = tr.get("dram_bytes_per_launch")
+    tr = None if coal else recorded_traffic(kern_name, name)
+    traffic = tr.get("dram_bytes_per_launch") if tr is not None else None
 
-    # e2e through the public API: every step copies its inputs from pinned host
-    # memory and reads its combined output back.  Steps are pipelined on three
-    # streams (H2D of step i+1 and D2H of step i-1 overlap the kernels of step
-    # i), with double-buffered device inputs and outputs.  No flush here: one
-    # step's footprint (x, recv, y, out) is larger than L2.  A step's inputs
-    # (x, topk_idx, topk_w) sit in one pinned host slab and go over in one
-    # copy, into one device slab that the calls take views of: each separate
-    # small copy cost the host link ~7.5 us per step (measured: 112.9 us per
-    # step with three copies, 105.4 with two).
-    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    XB, IB, WB = T * H * 2, T * k * 4, T * k * 4
-    in_h = torch.empty(XB + IB + WB, dtype=torch.uint8).pin_memory()
-    in_h[:XB].copy_(torch.from_numpy(w.x.view(np.uint8).reshape(-1)))
-    in_h[XB:XB + IB].copy_(torch.from_numpy(w.topk_idx.view(np.uint8).reshape(-1)))
-    in_h[XB + IB:].copy_(torch.from_numpy(w.topk_w.view(np.uint8).reshape(-1)))
-    in_d = [torch.empty(XB + IB + WB, dtype=torch.uint8, device=dev) for _ in range(2)]
-    out_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    xb = [d[:XB].view(torch.bfloat16).view(T, H) for d in in_d]
-    ib = [d[XB:XB + IB].view(torch.int32).view(T, k) for d in in_d]
-    wb = [d[XB + IB:].view(torch.float32).view(T, k) for d in in_d]
-    ob = [out, torch.empty_like(out)]
-    rq = (dict(recv_q=recv_q, recv_scales=recv_s) if fp8
-          else (dict(recv_c=recv) if coal else dict(recv=recv)))
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    launches = b.launches_per_step() * args.steps
+    e2e = e2e_leg(b, args, world)
+    headline = per_config_entry(b, r, peak)
+    headline["clocks"] = r["clocks"]
+    x_host = y_host = None
+    want_cpu = not args.no_cpu_baseline and world == 1 and rank == 0 and not coal
+    if want_cpu:
+        x_host, y_host = host_bits(b.x), host_bits(b.y)
+    w_head = b.w
+    Nc = b.Nc
+    del b
+    torch.cuda.empty_cache()
 
-    def e2e_run(n):
-        h2d_done = [torch.cuda.Event() for _ in range(n)]
-        comp_done = [torch.cuda.Event() for _ in range(n)]
-        d2h_done = [torch.cuda.Event() for _ in range(n)]
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        t0.record(h2d_s)
-        for i in range(n):
-            b = i % 2
-            with torch.cuda.stream(h2d_s):
-                if i >= 2:
-                    h2d_s.wait_event(comp_done[i - 2])
-                in_d[b].copy_(in_h, non_blocking=True)
-                h2d_done[i].record(h2d_s)
-            stream.wait_event(h2d_done[i])
-            if i >= 2:
-                stream.wait_event(d2h_done[i - 2])
-            if fused_front:
-                m.moe_layout_dispatch(xb[b], ib[b], E, R, workspace=ws, out=lay, err_word=err,
-                                      stream=stream, **rq)
-                m.moe_combine(y, lay.slot_of, wb[b], out=ob[b], err_word=err, stream=stream)
-            elif coal:
-                m.moe_layout(ib[b], E, R, workspace=ws, err_word=err, out=lay, stream=stream)
-                m.moe_layout_coalesced(ib[b], lay.slot_of, E, R, workspace=wsc, err_word=err,
-                                       out=co, stream=stream)
-                if fp8:
-                    m.moe_dispatch_quant_coalesced(xb[b], co.crow, rows, err_word=err,
-                                                   stream=stream, **rq)
-                else:
-                    m.moe_dispatch_coalesced(xb[b], co.crow, rows, err_word=err, stream=stream,
-                                             **rq)
-                m.moe_combine_coalesced(y, lay.slot_of, wb[b], co, rows, partial=partial,
-                                        out=ob[b], err_word=err, stream=stream)
-            else:
-                m.moe_layout(ib[b], E, R, workspace=ws, err_word=err, out=lay, stream=stream)
-                m.moe_dispatch_quant(xb[b], lay.slot_of, err_word=err, stream=stream, **rq)
-                m.moe_combine(y, lay.slot_of, wb[b], out=ob[b], err_word=err, stream=stream)
-            comp_done[i].record(stream)
-            with torch.cuda.stream(d2h_s):
-                d2h_s.wait_event(comp_done[i])
-                out_h[b].copy_(ob[b], non_blocking=True)
-                d2h_done[i].record(d2h_s)
-        d2h_s.wait_event(d2h_done[n - 1])
-        t1.record(d2h_s)
-        torch.cuda.synchronize()
-        return t0.elapsed_time(t1)
-
-    e2e_run(3)  # warm-up
-    e2e_ms = allreduce_max(e2e_run(e2e_steps)) / e2e_steps
-    bits = m.moe_read_error(err)
-    if bits:
-        raise RuntimeError(f"device error bits {bits:#x}")
-    # the last output read back must be the combine of the resident inputs
-    if coal:
-        ref, _ = m.moe_combine_coalesced(y, lay.slot_of, wt, co, rows, partial=partial)
-    else:
-        ref = m.moe_combine(y, lay.slot_of, wt)
-    torch.cuda.synchronize()
-    if not torch.equal(out_h[(e2e_steps - 1) % 2].view(torch.int16), ref.cpu().view(torch.int16)):
-        raise RuntimeError("e2e output differs from the combine of the resident inputs")
-    h2d = in_h.numel()  # x, topk_idx and topk_w
-    d2h = out.numel() * 2
+    # the other workloads of the target (configs 1-4), each through the same
+    # timed loop and L2 regime, one after the other
+    per_config = {name: headline}
+    host_inputs = {name: (w_head, x_host, y_host)}
+    if not args.no_per_config and not coal:
+        for other in args.per_config.split(","):
+            if not other or other == name:
+                continue
+            bo = StepBench(other, dev, args.seed + rank, "plain", m)
+            ro = bo.timed(args.steps, args.warmup, clocks_uuid=uuid)
+            per_config[other] = per_config_entry(bo, ro, peak)
+            per_config[other]["clocks"] = ro["clocks"]
+            if want_cpu:
+                host_inputs[other] = (bo.w, host_bits(bo.x), host_bits(bo.y))
+            del bo
+            torch.cuda.empty_cache()
+    smi.mark_stop()
+    smi.__exit__(None, None, None)
 
     if rank != 0:
         return
+    clocks = r["clocks"] or {"samples": 0}
+    if not clocks.get("samples"):
+        clocks = smi.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -674,34 +834,138 @@ def run_gpu(args):
                    "tokens_per_step": T, "variant": args.variant,
                    "l2": "flushed every step outside the events: 2xL2 written before layout+"
                          "dispatch, 4xL2 read before combine",
+                   "inputs": "routing from workloads/gen.py (seed 0); x ~ N(0,1) and the expert "
+                             "outputs drawn on the device with torch's seeded generator",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": kern_name, "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "traffic_source": tr.get("capture") if tr is not None else None,
                      "algorithmic_bytes": dom_bytes, "duration_ms": dom_ms,
                      "duration_source": source},
-        "segments_ms": {"layout+" + d_name: statistics.mean(t_front), "combine": avg_c},
-        "kernels_ms": {"layout": statistics.mean(t_layout), d_name: avg_d, "combine": avg_c},
+        "segments_ms": {"layout+" + b_dname(fp8, coal): statistics.mean(t_front),
+                        "combine": avg_c},
+        "kernels_ms": {"layout": statistics.mean(r["t_layout"]), b_dname(fp8, coal): avg_d,
+                       "combine": avg_c},
         "step_hbm_gbs": (None if coal else
                          step_bytes(T, H, k, E, R, fp8) / (ms_per_step / 1000.0) / 1e9),
-        "wall_ms_per_step_incl_flush": 1000.0 * wall / args.steps,
-        "e2e": {"value": world * T / (e2e_ms / 1000.0), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "steps": e2e_steps,
-                "how": "public API; one H2D copy per step (x, topk_idx, topk_w in one pinned "
-                       "slab); H2D of step i+1 and D2H of step i-1 overlap step i's kernels "
-                       "(three streams, double-buffered inputs/outputs); one step's footprint "
-                       "exceeds L2"},
-        # layout, dispatch, combine; the coalesced step adds the coalesced
-        # layout (a second launch when k does not divide 32)
-        "gpu_launches": ((4 if 32 % k == 0 else 5) if coal else 3) * args.steps,
-        "clocks": clocks.summary(),
+        "wall_ms_per_step_incl_flush": 1000.0 * r["wall"] / args.steps,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "clocks_window": smi.summary(),
+        "per_config": per_config,
     }
     if coal:
         line["config"]["coalesced_rows"] = {"N": N, "Nc": Nc}
-    if not args.no_cpu_baseline and world == 1 and not coal:
-        line["cpu_baseline"] = cpu_baseline(name, args.cpu_budget)
+    if want_cpu:
+        wh, xh, yh = host_inputs[name]
+        line["cpu_baseline"] = cpu_baseline(name, args.cpu_budget, wh, xh, yh)
+        for nm, (wo, xo, yo) in host_inputs.items():
+            per_config[nm]["oracle_1core"] = oracle_op_times(nm, xo, yo, wo)
     print(json.dumps(line), flush=True)
+
+
+def b_dname(fp8, coal):
+    return (("dispatch_fp8_coalesced" if fp8 else "dispatch_coalesced") if coal
+            else ("dispatch_fp8" if fp8 else "dispatch_bf16"))
+
+
+def e2e_leg(b: StepBench, args, world):
+    """The step through the public API with host buffers: every step copies its
+    inputs from pinned host memory and reads its combined output back.  Steps
+    are pipelined on three streams (H2D of step i+1 and D2H of step i-1
+    overlap step i's kernels), with double-buffered device inputs and
+    outputs.  No flush here: one step's footprint (x, recv, y, out) is larger
+    than L2.  A step's inputs (x, topk_idx, topk_w) sit in one pinned host slab
+    and go over in one copy, into one device slab that the calls take views
+    of: each separate small copy cost the host link ~7.5 us per step."""
+    import torch
+    m, dev, stream = b.m, b.dev, b.stream
+    T, H, k, E, R = b.T, b.H, b.k, b.E, b.R
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    XB, IB, WB = T * H * 2, T * k * 4, T * k * 4
+    in_h = torch.empty(XB + IB + WB, dtype=torch.uint8).pin_memory()
+    in_h[:XB].copy_(b.x.view(torch.uint8).reshape(-1).cpu())
+    in_h[XB:XB + IB].copy_(torch.from_numpy(b.w.topk_idx.view(np.uint8).reshape(-1)))
+    in_h[XB + IB:].copy_(torch.from_numpy(b.w.topk_w.view(np.uint8).reshape(-1)))
+    in_d = [torch.empty(XB + IB + WB, dtype=torch.uint8, device=dev) for _ in range(2)]
+    out_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xb = [d[:XB].view(torch.bfloat16).view(T, H) for d in in_d]
+    ib = [d[XB:XB + IB].view(torch.int32).view(T, k) for d in in_d]
+    wb = [d[XB + IB:].view(torch.float32).view(T, k) for d in in_d]
+    ob = [b.out, torch.empty_like(b.out)]
+    y, lay, ws, err = b.y, b.lay, b.ws, b.err
+    rq = (dict(recv_q=b.recv_q, recv_scales=b.recv_s) if b.fp8
+          else (dict(recv_c=b.recv) if b.coal else dict(recv=b.recv)))
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def run(n):
+        h2d_done = [torch.cuda.Event() for _ in range(n)]
+        comp_done = [torch.cuda.Event() for _ in range(n)]
+        d2h_done = [torch.cuda.Event() for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(h2d_s)
+        for i in range(n):
+            j = i % 2
+            with torch.cuda.stream(h2d_s):
+                if i >= 2:
+                    h2d_s.wait_event(comp_done[i - 2])
+                in_d[j].copy_(in_h, non_blocking=True)
+                h2d_done[i].record(h2d_s)
+            stream.wait_event(h2d_done[i])
+            if i >= 2:
+                stream.wait_event(d2h_done[i - 2])
+            if b.fused_front:
+                m.moe_layout_dispatch(xb[j], ib[j], E, R, workspace=ws, out=lay, err_word=err,
+                                      stream=stream, **rq)
+                m.moe_combine(y, lay.slot_of, wb[j], out=ob[j], err_word=err, stream=stream)
+            elif b.coal:
+                co = b.co
+                m.moe_layout(ib[j], E, R, workspace=ws, err_word=err, out=lay, stream=stream)
+                m.moe_layout_coalesced(ib[j], lay.slot_of, E, R, workspace=b.wsc, err_word=err,
+                                       out=co, stream=stream)
+                if b.fp8:
+                    m.moe_dispatch_quant_coalesced(xb[j], co.crow, b.rows, err_word=err,
+                                                   stream=stream, **rq)
+                else:
+                    m.moe_dispatch_coalesced(xb[j], co.crow, b.rows, err_word=err,
+                                             stream=stream, **rq)
+                m.moe_combine_coalesced(y, lay.slot_of, wb[j], co, b.rows, partial=b.partial,
+                                        out=ob[j], err_word=err, stream=stream)
+            else:
+                m.moe_layout(ib[j], E, R, workspace=ws, err_word=err, out=lay, stream=stream)
+                m.moe_dispatch_quant(xb[j], lay.slot_of, err_word=err, stream=stream, **rq)
+                m.moe_combine(y, lay.slot_of, wb[j], out=ob[j], err_word=err, stream=stream)
+            comp_done[i].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(comp_done[i])
+                out_h[j].copy_(ob[j], non_blocking=True)
+                d2h_done[i].record(d2h_s)
+        d2h_s.wait_event(d2h_done[n - 1])
+        t1.record(d2h_s)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    run(3)  # warm-up
+    e2e_ms = allreduce_max(run(steps)) / steps
+    b.check_errors("in the e2e leg")
+    # the last output read back must be the combine of the resident inputs
+    if b.coal:
+        ref, _ = m.moe_combine_coalesced(y, lay.slot_of, b.wt, b.co, b.rows, partial=b.partial)
+    else:
+        ref = m.moe_combine(y, lay.slot_of, b.wt)
+    torch.cuda.synchronize()
+    if not torch.equal(out_h[(steps - 1) % 2].view(torch.int16), ref.cpu().view(torch.int16)):
+        raise RuntimeError("e2e output differs from the combine of the resident inputs")
+    return {"value": world * T / (e2e_ms / 1000.0), "unit": UNIT,
+            "h2d_bytes_per_step": in_h.numel(), "d2h_bytes_per_step": b.out.numel() * 2,
+            "ms_per_step": e2e_ms, "steps": steps,
+            "how": "public API; one H2D copy per step (x, topk_idx, topk_w in one pinned "
+                   "slab); H2D of step i+1 and D2H of step i-1 overlap step i's kernels "
+                   "(three streams, double-buffered inputs/outputs); one step's footprint "
+                   "exceeds L2"}
 
 
 # ------------------------------------------------------------------ kernel table
@@ -843,6 +1107,10 @@ def main(argv=None):
     p.add_argument("--ref-tokens", type=int, default=64,
                    help="tokens per oracle step in --impl reference")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--per-config", default=PER_CONFIG,
+                   help="comma-separated workloads timed after the headline, each through "
+                        "the same loop, reported in the line's per_config block")
+    p.add_argument("--no-per-config", action="store_true")
     p.add_argument("--variant", choices=["plain", "coalesced"], default="plain",
                    help="plain: the hot path; coalesced: the rank-coalesced path")
     p.add_argument("--table", action="store_true",

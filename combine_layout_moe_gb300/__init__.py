@@ -22,6 +22,9 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_BAD_INDEX, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, \
     MOE_ERR_UNSUPPORTED, MOE_ERR_INTEGRITY = range(7)
 MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
 MOE_ERRBIT_BAD_INDEX, MOE_ERRBIT_TIMEOUT, MOE_ERRBIT_SENTINEL, MOE_ERRBIT_CHECKSUM = 0x1, 0x2, 0x4, 0x8
+MOE_ERRBIT_LAUNCH = 0x10
+MOE_LAYOUT_FORM_NONE, MOE_LAYOUT_FORM_SINGLE, MOE_LAYOUT_FORM_CLUSTER, \
+    MOE_LAYOUT_FORM_COOPERATIVE, MOE_LAYOUT_FORM_FUSED = range(5)
 MOE_SYNC_WORD, MOE_SYNC_SENTINEL, MOE_SYNC_BATCH, MOE_SYNC_BARRIER = range(4)
 MOE_MAX_EXPERTS = 1024
 
@@ -40,6 +43,7 @@ SIGNATURES = {
     "moe_read_error": ([_U32P, _I, _P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "moe_layout_noalloc": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_sync_words": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
+    "moe_layout_last_form": ([], ctypes.c_int),
     "moe_combine_backward": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_dispatch_backward": ([_I, _I, _I, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_layout_coalesced": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P],
@@ -108,6 +112,11 @@ def moe_abi_version() -> int:
 
 def moe_status_string(status: int) -> str:
     return _lib.moe_status_string(status).decode()
+
+
+def moe_layout_last_form() -> int:
+    """MOE_LAYOUT_FORM_* of the layout kernel this host thread launched last."""
+    return int(_lib.moe_layout_last_form())
 
 
 def new_error_word(device=None) -> torch.Tensor:

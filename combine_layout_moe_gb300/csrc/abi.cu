@@ -351,6 +351,8 @@ moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t stream, ui
     }
     if (bits_out)
         *bits_out = bits;
+    if (bits & MOE_ERRBIT_LAUNCH)
+        return MOE_ERR_CUDA;
     if (bits & MOE_ERRBIT_TIMEOUT)
         return MOE_ERR_TIMEOUT;
     if (bits & MOE_ERRBIT_BAD_INDEX)

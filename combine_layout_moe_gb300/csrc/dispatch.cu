@@ -387,6 +387,11 @@ cudaError_t launch_layout_dispatch(int T, int H, int k, int E, int R, const int3
                                    int32_t *slot_of, int32_t *src_of, void *recv,
                                    void *workspace, uint32_t *err_word, cudaStream_t stream)
 {
+    // small batches: one kernel in which every CTA computes the layout itself
+    if (layout_dispatch_fused_fits(T, H, k, E))
+        return launch_layout_dispatch_fused(T, H, k, E, R, topk_idx, x, expert_counts,
+                                            expert_offsets, rank_offsets, slot_of, src_of, recv,
+                                            err_word, stream);
     cudaError_t e = launch_layout(T, k, E, R, topk_idx, expert_counts, expert_offsets,
                                   rank_offsets, slot_of, src_of, workspace, err_word, stream);
     if (e != cudaSuccess || T == 0)

@@ -10,10 +10,16 @@ namespace moe {
 
 size_t layout_workspace_bytes(int64_t N, int E);
 
+// clear_barrier: zero the workspace's grid-barrier head on the stream before
+// a launch in the grid-barrier form (the only form that reads it).
 cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
                           int32_t *expert_counts, int32_t *expert_offsets,
                           int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
-                          void *workspace, uint32_t *err_word, cudaStream_t stream);
+                          void *workspace, uint32_t *err_word, cudaStream_t stream,
+                          bool clear_barrier = false);
+
+// Records the layout form (MOE_LAYOUT_FORM_*) this host thread launched last.
+void note_layout_form(int form);
 
 cudaError_t launch_layout_coalesced(int T, int k, int E, int R, const int32_t *topk_idx,
                                     const int32_t *slot_of, int32_t *rank_counts_c,
@@ -35,6 +41,16 @@ cudaError_t launch_layout_dispatch(int T, int H, int k, int E, int R, const int3
                                    int32_t *expert_offsets, int32_t *rank_offsets,
                                    int32_t *slot_of, int32_t *src_of, void *recv,
                                    void *workspace, uint32_t *err_word, cudaStream_t stream);
+
+// The single-kernel layout + dispatch for small batches (layout_dispatch.cu):
+// whether a batch fits it, and its launch.
+bool layout_dispatch_fused_fits(int T, int H, int k, int E);
+cudaError_t launch_layout_dispatch_fused(int T, int H, int k, int E, int R,
+                                         const int32_t *topk_idx, const void *x,
+                                         int32_t *expert_counts, int32_t *expert_offsets,
+                                         int32_t *rank_offsets, int32_t *slot_of,
+                                         int32_t *src_of, void *recv, uint32_t *err_word,
+                                         cudaStream_t stream);
 
 cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
                                 uint8_t *recv_q, float *recv_scales, uint32_t *err_word,

@@ -5,20 +5,23 @@
 // Appendix D: the placement metadata is destination expert, per-expert counts,
 // prefix-sum offsets and token-local offsets.
 //
-// GPU design: one cooperative launch, one CTA per tile.  The (token, slot)
-// pairs i = t*k + j are cut into equal contiguous tiles of ~2048 pairs (at
-// most LAYOUT_MAX_TILES tiles), and each tile into equal warp spans (UBEP
+// GPU design: one launch, one 512-thread CTA per tile.  The (token, slot)
+// pairs i = t*k + j are cut into equal contiguous tiles of about 1024 pairs
+// (at most LAYOUT_MAX_TILES tiles), and each tile into equal warp spans (UBEP
 // section 3.3's token-level load partition).
 //   1. Each warp histograms its span into a private shared-memory row (the
-//      expert ids stay in registers); the CTA writes the row sums to its row of
-//      the tile-count table.
-//   2. Grid barrier (arrival count and generation in the workspace; bounded).
-//      With at most CLUSTER_MAX_TILES (16) tiles the grid is one thread-block
-//      cluster instead (sizes above 8 only where the GPU can place one): each CTA keeps its row in shared memory, a hardware
-//      cluster barrier replaces the grid barrier, and step 3 reads the other
-//      CTAs' rows through distributed shared memory (no table in global
-//      memory, no atomics, no polling).
-//   3. Each CTA column-sums the table (all tiles -> totals -> exclusive scan
+//      expert ids stay in registers); the CTA sums the rows into its tile's
+//      counts.
+//   2. The tiles' counts are exchanged.  One tile needs no exchange.  Up to
+//      CLUSTER_MAX_TILES (16) tiles the grid is one thread-block cluster
+//      (sizes above 8 only where the GPU can place one): each CTA keeps its
+//      counts in shared memory, a hardware cluster barrier publishes them, and
+//      step 3 reads the other CTAs' counts through distributed shared memory
+//      (no table in global memory, no atomics, no polling).  Beyond that the
+//      launch is cooperative: the counts go to a tile-count table in the
+//      workspace and a grid barrier (arrival count and generation in the
+//      workspace head, time-bounded) follows.
+//   3. Each CTA column-sums the counts (all tiles -> totals -> exclusive scan
 //      over experts; earlier tiles -> this tile's base), turns the per-warp
 //      histograms into per-warp cursors, and walks its span in order:
 //      slot = cursor[e] + number of lower lanes of the same 32-pair step with
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
         asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
         const int nread = min(tiles, (int)ncta);
         if (tid == 0 && (int)ncta != tiles)
-            report(err_word, MOE_ERRBIT_TIMEOUT);
+            report(err_word, MOE_ERRBIT_LAUNCH);
         for (int e = tid; e < E; e += LAYOUT_THREADS) {
             const uint32_t la = smem_addr(tsum + e);
             int32_t before = 0, total = 0;
@@ -255,6 +258,13 @@ __global__ void __launch_bounds__(LAYOUT_THREADS)
             pre[e] = before;
         }
         cluster_arrive();  // done reading the other CTAs' shared memory
+        if ((int)ncta != tiles) {
+            // a cluster of another size: the sums are partial, so write no
+            // offsets or slots; still wait, so that no CTA leaves while
+            // another may read its tsum
+            cluster_wait();
+            return;
+        }
     } else if (tiles > 1) {
         const int P = E >= LAYOUT_THREADS ? 1 : LAYOUT_THREADS / E;
         const int part = tid / E;
@@ -433,6 +443,12 @@ size_t layout_workspace_bytes(int64_t N, int E)
     return LAYOUT_BARRIER_BYTES + bytes;
 }
 
+// The form of the layout kernel that this host thread launched last
+// (MOE_LAYOUT_FORM_*), for moe_layout_last_form().
+static thread_local int g_last_form = MOE_LAYOUT_FORM_NONE;
+
+void note_layout_form(int form) { g_last_form = form; }
+
 template <int NBITS, bool COAL>
 static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, int k,
                                    const LayoutPlan &p,
@@ -440,7 +456,8 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, 
                                    int32_t *tile_counts, int32_t *expert_counts,
                                    int32_t *expert_offsets, int32_t *rank_offsets,
                                    int32_t *slot_of, int32_t *src_of, const int32_t *plain_slot,
-                                   int32_t *expand, uint32_t *err_word, cudaStream_t stream)
+                                   int32_t *expand, uint32_t *err_word, bool clear_barrier,
+                                   cudaStream_t stream)
 {
     const size_t smem = layout_smem(E);
     cudaError_t e = cudaSuccess;
@@ -496,10 +513,19 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, 
                 (void)cudaGetLastError();
                 e = launch(1, 1);  // without the programmatic attribute
             }
-            if (e == cudaSuccess)
+            if (e == cudaSuccess) {
+                note_layout_form(MOE_LAYOUT_FORM_CLUSTER);
                 return e;
+            }
             (void)cudaGetLastError();  // no cluster of this size: the cooperative form below
         }
+    }
+    if (clear_barrier && p.tiles > 1) {
+        // only the grid-barrier form reads the barrier head: a caller that
+        // cannot vouch for it being zero has it cleared here, on the stream
+        e = cudaMemsetAsync(barrier, 0, 8, stream);
+        if (e != cudaSuccess)
+            return e;
     }
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
@@ -509,6 +535,8 @@ static cudaError_t launch_layout_t(int64_t N, int E, int R, int e_real, int El, 
         (void)cudaGetLastError();
         e = launch(0, 1);
     }
+    if (e == cudaSuccess)
+        note_layout_form(p.tiles == 1 ? MOE_LAYOUT_FORM_SINGLE : MOE_LAYOUT_FORM_COOPERATIVE);
     return e;
 }
 
@@ -520,10 +548,11 @@ static cudaError_t launch_keys(int T, int k, int K, int R, int e_real, int El,
                                const int32_t *topk_idx, int32_t *counts, int32_t *offsets,
                                int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
                                const int32_t *plain_slot, int32_t *expand, void *workspace,
-                               uint32_t *err_word, cudaStream_t stream)
+                               uint32_t *err_word, bool clear_barrier, cudaStream_t stream)
 {
     const int64_t N = (int64_t)T * k;
     if (N == 0) {
+        note_layout_form(MOE_LAYOUT_FORM_NONE);
         cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * K, stream);
         if (e == cudaSuccess)
             e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (K + 1), stream);
@@ -543,7 +572,8 @@ static cudaError_t launch_keys(int T, int k, int K, int R, int e_real, int El,
     case B:                                                                                    \
         return launch_layout_t<B, COAL>(N, K, R, e_real, El, k, p, topk_idx, barrier,          \
                                         tile_counts, counts, offsets, rank_offsets, slot_of,   \
-                                        src_of, plain_slot, expand, err_word, stream);
+                                        src_of, plain_slot, expand, err_word,          \
+                                        clear_barrier, stream);
         MOE_LAYOUT_CASE(0)
         MOE_LAYOUT_CASE(1)
         MOE_LAYOUT_CASE(2)
@@ -564,11 +594,12 @@ static cudaError_t launch_keys(int T, int k, int K, int R, int e_real, int El,
 cudaError_t launch_layout(int T, int k, int E, int R, const int32_t *topk_idx,
                           int32_t *expert_counts, int32_t *expert_offsets,
                           int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
-                          void *workspace, uint32_t *err_word, cudaStream_t stream)
+                          void *workspace, uint32_t *err_word, cudaStream_t stream,
+                          bool clear_barrier)
 {
     return launch_keys<false>(T, k, E, R, E, E / R, topk_idx, expert_counts, expert_offsets,
                               rank_offsets, slot_of, src_of, nullptr, nullptr, workspace,
-                              err_word, stream);
+                              err_word, clear_barrier, stream);
 }
 
 // Non-owner slots take their owner's coalesced row; expand[slot_of[i]] = crow[i].
@@ -616,7 +647,7 @@ cudaError_t launch_layout_coalesced(int T, int k, int E, int R, const int32_t *t
     cudaError_t e = launch_keys<true>(T, k, R, R, E, E / R, topk_idx, rank_counts_c,
                                       rank_offsets_c, nullptr, crow, src_pair_c,
                                       fused ? slot_of : nullptr, fused ? expand : nullptr,
-                                      workspace, err_word, stream);
+                                      workspace, err_word, false, stream);
     const int64_t N = (int64_t)T * k;
     if (e != cudaSuccess || N == 0 || fused)
         return e;
@@ -630,3 +661,5 @@ cudaError_t launch_layout_coalesced(int T, int k, int E, int R, const int32_t *t
 }
 
 }  // namespace moe
+
+extern "C" MOE_API int moe_layout_last_form(void) { return moe::g_last_form; }

@@ -59,6 +59,9 @@ typedef enum moe_out_dtype { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 } moe_out_dtype;
 #define MOE_ERRBIT_TIMEOUT 0x2u
 #define MOE_ERRBIT_SENTINEL 0x4u
 #define MOE_ERRBIT_CHECKSUM 0x8u
+#define MOE_ERRBIT_LAUNCH 0x10u /* a kernel found itself launched in a shape it   */
+                                /* cannot serve (a cluster of the wrong size);    */
+                                /* it wrote no outputs                            */
 
 /* how moe_dispatch_combine_flagged's readers learn that data has arrived */
 typedef enum moe_sync_mode {
@@ -137,13 +140,18 @@ MOE_API moe_status moe_dispatch(int T, int H, int k, const void *x, const int32_
 
 /*
  * moe_layout_dispatch -- moe_layout followed by moe_dispatch (bf16), with the
- * dispatch's first loads of x overlapping the layout.
+ * dispatch's loads of x overlapping the layout.
  *
  * UBEP, section 3.2 (kernel decomposition: token sending overlaps the count
  * and scan instead of waiting behind them).  Same arguments, outputs, rules
- * and errors as moe_layout and moe_dispatch called in turn on `stream`.  The
- * dispatch kernel may read x while the layout kernel still runs, which is
- * safe here because x must be complete before this call, as for moe_dispatch.
+ * and errors as moe_layout and moe_dispatch called in turn on `stream`.
+ * Small batches (T*k <= 16384, each SM's share of x within shared memory,
+ * k <= 32) run as one kernel: every CTA loads its share of x, counts the
+ * whole batch's ids itself while those loads land, and stores its rows to
+ * their slots -- no exchange between CTAs and no second launch; the workspace
+ * is then not touched.  Larger batches run the layout kernel, then a dispatch
+ * kernel that reads x while the layout still runs.  Either way x must be
+ * complete before this call, as for moe_dispatch.
  */
 MOE_API moe_status moe_layout_dispatch(int T, int H, int k, int E, int R,
                                const int32_t *topk_idx, const void *x,
@@ -442,12 +450,43 @@ MOE_API moe_status moe_layout_noalloc(int T, int k, int E, int R, const int32_t 
 
 /*
  * moe_read_error -- synchronise `stream`, read the device error word into
- * *bits_out (may be NULL), clear it when `clear` is non-zero, and return
- * MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_TIMEOUT (timeout wins when both bits
- * are set).  MOE_ERR_CUDA if the synchronisation or copy fails.
+ * *bits_out (may be NULL), clear it when `clear` is non-zero, and return the
+ * status of the most serious bit set, in this order:
+ *   MOE_ERRBIT_LAUNCH                        -> MOE_ERR_CUDA
+ *   MOE_ERRBIT_TIMEOUT                       -> MOE_ERR_TIMEOUT
+ *   MOE_ERRBIT_BAD_INDEX                     -> MOE_ERR_BAD_INDEX
+ *   MOE_ERRBIT_SENTINEL, MOE_ERRBIT_CHECKSUM -> MOE_ERR_INTEGRITY
+ * and MOE_OK when no bit is set.  MOE_ERR_CUDA also if the synchronisation or
+ * the copy fails.  The error word is a separate argument of every call, not a
+ * part of a workspace: the dispatch and combine calls take no workspace, and
+ * one word can collect the errors of a whole step of calls.
  */
 MOE_API moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t stream,
                           uint32_t *bits_out);
+
+/*
+ * moe_layout_last_form -- diagnostic: which form of the layout kernel the most
+ * recent moe_layout, moe_layout_dispatch, moe_layout_coalesced or
+ * moe_layout_noalloc call made by this host thread launched.  The pages have
+ * no counterpart; tests use it to check that a given shape took the form
+ * they mean to exercise.
+ *   MOE_LAYOUT_FORM_NONE         nothing launched (T == 0, or no call yet)
+ *   MOE_LAYOUT_FORM_SINGLE       one CTA (at most one tile of pairs)
+ *   MOE_LAYOUT_FORM_CLUSTER      one thread-block cluster of 2..16 CTAs
+ *   MOE_LAYOUT_FORM_COOPERATIVE  a cooperative grid with a grid barrier in the
+ *                                workspace (more than 16 tiles, or a cluster
+ *                                the GPU could not place)
+ *   MOE_LAYOUT_FORM_FUSED        moe_layout_dispatch's single kernel, in
+ *                                which every CTA computes the whole layout
+ *                                itself (small batches; see there)
+ */
+#define MOE_LAYOUT_FORM_NONE 0
+#define MOE_LAYOUT_FORM_SINGLE 1
+#define MOE_LAYOUT_FORM_CLUSTER 2
+#define MOE_LAYOUT_FORM_COOPERATIVE 3
+#define MOE_LAYOUT_FORM_FUSED 4
+
+MOE_API int moe_layout_last_form(void);
 
 #ifdef __cplusplus
 }

@@ -87,11 +87,23 @@ FUZZ = [  # (seed, T, k, E, R)
 ]
 
 
+# The form each straddling shape must take on a GB300 (clusters of 9..16 CTAs
+# are non-portable sizes, which the launcher uses only where the GPU can place
+# them; GB300 can): a silent fall-back to the grid barrier would still pass the
+# parity check, so the form is checked as well.
+FUZZ_FORM = {16: "CLUSTER", 17: "CLUSTER", 18: "CLUSTER", 19: "CLUSTER", 20: "CLUSTER",
+             21: "COOPERATIVE", 1: "SINGLE", 2: "SINGLE", 3: "SINGLE", 5: "SINGLE",
+             12: "COOPERATIVE"}
+
+
 @pytest.mark.parametrize("case", FUZZ, ids=[f"s{c[0]}_T{c[1]}_k{c[2]}_E{c[3]}" for c in FUZZ])
 def test_layout_fuzz(case):
     seed, T, k, E, R = case
     w = random_case(seed, T, 8, k, E, R)
     assert_layout_equal(w.topk_idx, E, R)
+    if seed in FUZZ_FORM:
+        m = cl()
+        assert m.moe_layout_last_form() == getattr(m, "MOE_LAYOUT_FORM_" + FUZZ_FORM[seed])
 
 
 def test_layout_all_one_expert_and_hot_expert():
@@ -356,3 +368,58 @@ def test_layout_dispatch_fuzz(case):
     o = oracle.layout(w.topk_idx, E, R)
     assert np.array_equal(lay.slot_of.cpu().numpy(), o[3])
     assert np.array_equal(bits(recv), oracle.dispatch(w.x, o[3]))
+
+
+# Shapes of the single-kernel layout + dispatch (every CTA counts the whole
+# batch itself; at most 16384 pairs, each CTA's share of x resident in shared
+# memory): one token, ragged H, rows split in two units, k = 32 with the
+# largest expert count, fewer units than SMs, a 2048-token decode batch (the
+# largest share of x a CTA holds), and k = 5.  (seed, T, H, k, E, R)
+FUSED = [(81, 1, 8, 1, 1, 1), (82, 7, 7176, 8, 256, 32), (83, 1024, 7168, 8, 256, 32),
+         (84, 2048, 7168, 8, 256, 32), (85, 500, 12288, 4, 64, 8), (86, 512, 1000, 32, 1024, 16),
+         (87, 3000, 512, 5, 7, 7), (88, 160, 4096, 2, 8, 8)]
+
+
+@pytest.mark.parametrize("case", FUSED, ids=[f"s{c[0]}_T{c[1]}_H{c[2]}_k{c[3]}" for c in FUSED])
+@pytest.mark.parametrize("aligned_ids", [True, False])
+def test_layout_dispatch_single_kernel(case, aligned_ids):
+    m = cl()
+    seed, T, H, k, E, R = case
+    w = random_case(seed, T, H, k, E, R)
+    if aligned_ids:
+        idx = i32_dev(w.topk_idx)
+    else:  # ids 4 bytes past a 16-byte boundary: the kernel's scalar path
+        buf = torch.zeros(T * k + 1, dtype=torch.int32, device="cuda")
+        buf[1:] = i32_dev(w.topk_idx).view(-1)
+        idx = buf[1:].view(T, k)
+        assert idx.data_ptr() % 16 == 4
+    err = m.new_error_word()
+    lay, recv = m.moe_layout_dispatch(bf16_dev(w.x), idx, E, R, err_word=err)
+    assert m.moe_layout_last_form() == m.MOE_LAYOUT_FORM_FUSED
+    torch.cuda.synchronize()
+    assert m.moe_read_error(err) == 0
+    o = oracle.layout(w.topk_idx, E, R)
+    for name, a, b in zip(["expert_counts", "expert_offsets", "rank_offsets", "slot_of", "src_of"],
+                          lay, o):
+        assert np.array_equal(a.cpu().numpy(), b), name
+    assert np.array_equal(bits(recv), oracle.dispatch(w.x, o[3]))
+
+
+def test_layout_dispatch_single_kernel_bad_id():
+    m = cl()
+    w = random_case(89, 300, 256, 4, 16, 4)
+    idx = w.topk_idx.copy()
+    idx[7, 2] = 16          # one past the last expert
+    idx[200, 0] = -3
+    err = m.new_error_word()
+    lay, recv = m.moe_layout_dispatch(bf16_dev(w.x), i32_dev(idx), 16, 4, err_word=err)
+    assert m.moe_layout_last_form() == m.MOE_LAYOUT_FORM_FUSED
+    assert m.moe_read_error(err) == m.MOE_ERRBIT_BAD_INDEX
+    so = lay.slot_of.cpu().numpy()
+    assert so[7, 2] == -1 and so[200, 0] == -1
+    # the valid pairs still take the slots of the stable order over valid ids
+    good = (idx >= 0) & (idx < 16)
+    order = np.argsort(np.where(good, idx, 1 << 20).ravel(), kind="stable")[:good.sum()]
+    want = np.full(idx.size, -1, np.int64)
+    want[order] = np.arange(good.sum())
+    assert np.array_equal(so.ravel(), want)

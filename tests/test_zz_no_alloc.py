@@ -34,19 +34,27 @@ def _noalloc_via_abi(m, idx, E, R, out, err):
 
 def test_noalloc_layout_matches_moe_layout_on_consecutive_calls():
     import combine_layout_moe_gb300 as m
+    import oracle
     # the grid-barrier form (which uses the fixed array), clusters of 8 and 16
     # CTAs (which do not), then the grid-barrier form again
-    cases = [make_workload("glm45_air"), make_workload("dsv3_decode"),
-             random_case(78, 2048, 8, 8, 256, 32), random_case(77, 3000, 8, 6, 40, 8)]
+    cases = [(make_workload("glm45_air"), m.MOE_LAYOUT_FORM_COOPERATIVE),
+             (make_workload("dsv3_decode"), m.MOE_LAYOUT_FORM_CLUSTER),
+             (random_case(78, 2048, 8, 8, 256, 32), m.MOE_LAYOUT_FORM_CLUSTER),
+             (random_case(77, 3000, 8, 6, 40, 8), m.MOE_LAYOUT_FORM_COOPERATIVE)]
     err = m.new_error_word()
-    for w in cases:                                   # two and more calls in a row
+    for w, form in cases:                             # two and more calls in a row
         idx = torch.from_numpy(w.topk_idx).cuda()
         ref = m.moe_layout(idx, w.E, w.R)
         got = _empty_layout(m, w.T, w.k, w.E, w.R)
         _noalloc_via_abi(m, idx, w.E, w.R, got, err)
+        assert m.moe_layout_last_form() == form
         torch.cuda.synchronize()
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+        # and against the oracle directly: counts, offsets, rank offsets,
+        # slot map and its inverse
+        for a, b in zip(got, oracle.layout(w.topk_idx, w.E, w.R)):
+            assert np.array_equal(a.cpu().numpy().reshape(b.shape), b)
     assert m.moe_read_error(err) == 0
 
 
@@ -55,10 +63,13 @@ def test_noalloc_layout_repeated_same_input_and_python_binding():
     w = make_workload("mixtral")
     idx = torch.from_numpy(w.topk_idx).cuda()
     ref = m.moe_layout(idx, w.E, w.R)
+    import oracle
+    want = oracle.layout(w.topk_idx, w.E, w.R)
     for _ in range(2):
         got = m.moe_layout_noalloc(idx, w.E, w.R, out=_empty_layout(m, w.T, w.k, w.E, w.R))
         torch.cuda.synchronize()
         assert all(torch.equal(a, b) for a, b in zip(got, ref))
+        assert all(np.array_equal(a.cpu().numpy().reshape(b.shape), b) for a, b in zip(got, want))
 
 
 def test_noalloc_rejects_tables_beyond_the_fixed_scratch():

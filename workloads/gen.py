@@ -176,3 +176,22 @@ def random_case(seed: int, T: int, H: int, k: int, E: int, R: int,
                   topk_idx=np.ascontiguousarray(idx), topk_w=np.ascontiguousarray(w),
                   seed=seed)
     return wl
+
+
+def device_inputs(w: Workload, device, seed: Optional[int] = None):
+    """x [T, H] and expert outputs y [T*k, H], bf16 tensors drawn on `device`
+    with torch's seeded generator, for benchmarks whose inputs are too large
+    to draw quickly on the host.  Same distributions as `Workload.x` (N(0,1)
+    rounded to bf16, nearest-even) and `expert_output` (random sign, 7-bit
+    mantissa, exponent uniform over 2^-7 .. 2^2), not the same values."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(w.seed if seed is None else seed) * 7919 + 17)
+    x = torch.randn((w.T, w.H), generator=g, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    r = torch.randint(0, 1 << 31, (w.N, w.H), generator=g, device=device, dtype=torch.int32)
+    sign = (r & 1) << 15
+    mant = (r >> 1) & 0x7F
+    expo = (120 + (r >> 8) % 10) << 7
+    y = (sign | expo | mant).to(torch.int16).view(torch.bfloat16)
+    return x, y
