@@ -59,11 +59,14 @@ def _bind(path: str) -> ctypes.CDLL:
     L.oracle_dispatch_coalesced.argtypes = [I, I, I, P, P, P]
     L.oracle_combine_coalesced_pre.argtypes = [I, I, I, P, P, P, P, I, P]
     L.oracle_combine_coalesced_post.argtypes = [I, I, I, P, P, I, P, I]
+    L.oracle_ep_dispatch.argtypes = [I, P, I, I, I, P, P, P, P, P, P]
+    L.oracle_ep_combine.argtypes = [I, P, I, I, I, P, P, P, P, I]
     for f in ("oracle_layout", "oracle_dispatch", "oracle_dispatch_quant",
               "oracle_combine", "oracle_combine_f64", "oracle_abi_version",
               "oracle_combine_backward", "oracle_dispatch_backward",
               "oracle_layout_coalesced", "oracle_dispatch_coalesced",
-              "oracle_combine_coalesced_pre", "oracle_combine_coalesced_post"):
+              "oracle_combine_coalesced_pre", "oracle_combine_coalesced_post",
+              "oracle_ep_dispatch", "oracle_ep_combine"):
         getattr(L, f).restype = ctypes.c_int
     return L
 
@@ -257,6 +260,50 @@ def combine_coalesced_post(partial: np.ndarray, crow: np.ndarray, out_dtype: str
     _check(lib().oracle_combine_coalesced_post(T, H, k, _p(p), _p(cr), p.shape[0], _p(out),
                                                0 if out_dtype == "bf16" else 1))
     return out
+
+
+def ep_dispatch(idx_per_rank, x_per_rank, E: int):
+    """Expert-parallel dispatch across W = len(idx_per_rank) ranks.  Each
+    rank's ids are int32 [T_s, k] and rows uint16 bf16 bits [T_s, H].  Returns
+    (recv_counts int32 [W(receiver), W(source), El], recv per receiver: a list
+    of uint16 [rows_d, H], src_pair per receiver: a list of int64 global pair
+    indices t*k + j, t counted over the ranks' tokens in rank order)."""
+    W = len(idx_per_rank)
+    k = idx_per_rank[0].shape[1]
+    H = x_per_rank[0].shape[1]
+    tok_off = np.zeros(W + 1, np.int64)
+    tok_off[1:] = np.cumsum([a.shape[0] for a in idx_per_rank])
+    idx = np.ascontiguousarray(np.concatenate(idx_per_rank).reshape(-1, k), dtype=np.int32)
+    x = np.ascontiguousarray(np.concatenate(x_per_rank).reshape(-1, H), dtype=np.uint16)
+    N = idx.size
+    counts = np.empty((W, W, max(E // W, 1)), np.int32)
+    base = np.empty(W + 1, np.int64)
+    src_pair = np.empty(max(N, 1), np.int64)
+    recv = np.empty((max(N, 1), H), np.uint16)
+    _check(lib().oracle_ep_dispatch(W, _p(tok_off), k, E, H, _p(idx), _p(x), _p(counts),
+                                    _p(base), _p(src_pair), _p(recv)))
+    return (counts, [recv[base[d]:base[d + 1]] for d in range(W)],
+            [src_pair[base[d]:base[d + 1]] for d in range(W)])
+
+
+def ep_combine(idx_per_rank, w_per_rank, y_per_receiver, E: int, out_dtype: str = "bf16"):
+    """The return path: y_per_receiver[d] holds receiver d's expert outputs in
+    its receive order (as ep_dispatch lays recv out).  Returns each rank's
+    combined rows: a list of uint16 bf16 bits [T_s, H] ('bf16') or float32
+    ('f32')."""
+    W = len(idx_per_rank)
+    k = idx_per_rank[0].shape[1]
+    H = y_per_receiver[0].shape[1]
+    tok_off = np.zeros(W + 1, np.int64)
+    tok_off[1:] = np.cumsum([a.shape[0] for a in idx_per_rank])
+    idx = np.ascontiguousarray(np.concatenate(idx_per_rank).reshape(-1, k), dtype=np.int32)
+    w = np.ascontiguousarray(np.concatenate(w_per_rank).reshape(-1, k), dtype=np.float32)
+    y = np.ascontiguousarray(np.concatenate(y_per_receiver).reshape(-1, H), dtype=np.uint16)
+    T = int(tok_off[W])
+    out = np.empty((T, H), np.uint16 if out_dtype == "bf16" else np.float32)
+    _check(lib().oracle_ep_combine(W, _p(tok_off), k, E, H, _p(idx), _p(w), _p(y), _p(out),
+                                   0 if out_dtype == "bf16" else 1))
+    return [out[tok_off[s]:tok_off[s + 1]] for s in range(W)]
 
 
 def e4m3_encode(f: np.ndarray) -> np.ndarray:

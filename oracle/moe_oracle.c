@@ -32,6 +32,12 @@
  *                          combine; one slot per rank to bf16(w*y) summed in
  *                          fp32; integer payloads give the exact sum; within
  *                          a derived bound of the binary64 sum
+ *   oracle_ep_dispatch     numpy stable argsort of all ranks' ids (the receive
+ *                          buffers, concatenated, are the single-GPU order of
+ *                          the concatenated tokens); per-source bincounts;
+ *                          a Python brute-force sort of (expert, source, t, j)
+ *   oracle_ep_combine      float64 closed form within the fp32 bound; the
+ *                          identity-expert round trip returns x
  */
 #include <float.h>
 #include <math.h>
@@ -567,6 +573,113 @@ int oracle_combine_coalesced_post(int T, int H, int k, const uint16_t *partial,
                 ((float *)out)[(int64_t)t * H + h] = acc;
         }
     }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Expert parallelism across W real ranks                                     */
+/*                                                                            */
+/* UBEP, section 2.3 and Figure 2: before dispatch each rank allocates a      */
+/* receive region partitioned by source rank and expert; senders place every  */
+/* token in the region of each expert it chose; the receiver learns the       */
+/* per-expert counts of every source and, in Phase 5, computes offsets from   */
+/* them and reorders the tokens contiguously per expert.  UBEP section 4:     */
+/* the receive address space is partitioned in advance.  StrataCL Appendix D: */
+/* per-expert counts and token-local offsets are the metadata that combine    */
+/* reuses to return rows.                                                     */
+/*                                                                            */
+/* Rank s holds the tokens [tok_off[s], tok_off[s+1]) of the concatenated     */
+/* arrays (topk_idx, x, topk_w are all ranks' rows, rank by rank).  Expert e  */
+/* lives on rank e / El, El = E / W.  Reading taken where the pages leave the */
+/* order open: the receiver's buffer holds, for each local expert el in       */
+/* order, the rows of source 0, then source 1, ..., each source's rows in its */
+/* own (token, slot) order.                                                   */
+/*   recv_counts [W][W][El]  recv_counts[(d*W + s)*El + el]: rows receiver d  */
+/*                           gets from source s for its local expert el       */
+/*   recv_base   [W+1]       first row of receiver d in recv; [W] = all rows  */
+/*   src_pair    [rows]      global pair t*k + j that each received row holds */
+/*   recv        [rows, H]   the received rows (bf16 bits)                    */
+/* ------------------------------------------------------------------------- */
+int oracle_ep_dispatch(int W, const int64_t *tok_off, int k, int E, int H,
+                       const int32_t *topk_idx, const uint16_t *x, int32_t *recv_counts,
+                       int64_t *recv_base, int64_t *src_pair, uint16_t *recv)
+{
+    if (W < 1 || k < 1 || E < 1 || E % W != 0 || H < 1 || tok_off[0] != 0)
+        return ORACLE_ERR_INVALID_ARG;
+    for (int s = 0; s < W; ++s)
+        if (tok_off[s + 1] < tok_off[s])
+            return ORACLE_ERR_INVALID_ARG;
+    const int El = E / W;
+    const int64_t T = tok_off[W];
+    for (int64_t i = 0; i < T * k; ++i)
+        if (topk_idx[i] < 0 || topk_idx[i] >= E)
+            return ORACLE_ERR_BAD_INDEX;
+    int64_t row = 0;
+    for (int d = 0; d < W; ++d) {
+        recv_base[d] = row;
+        for (int el = 0; el < El; ++el) {
+            const int e = d * El + el;
+            for (int s = 0; s < W; ++s) {
+                int32_t cnt = 0;
+                for (int64_t t = tok_off[s]; t < tok_off[s + 1]; ++t)
+                    for (int j = 0; j < k; ++j)
+                        if (topk_idx[t * k + j] == e) {
+                            src_pair[row] = t * k + j;
+                            memcpy(recv + row * H, x + t * H, sizeof(uint16_t) * (size_t)H);
+                            ++row;
+                            ++cnt;
+                        }
+                recv_counts[((int64_t)d * W + s) * El + el] = cnt;
+            }
+        }
+    }
+    recv_base[W] = row;
+    return ORACLE_OK;
+}
+
+/* The return path (combine across ranks): y holds the experts' outputs in the */
+/* receive buffers' order (the layout oracle_ep_dispatch gives recv).  Every   */
+/* token's output is the router-weighted sum of its k rows wherever they were  */
+/* received, with the precision of oracle_combine: fp32, one fused multiply-   */
+/* add per slot in slot order from +0, one rounding (HyperParallel-MoE         */
+/* sections 2.2 and 4.1).  out_dtype: 0 = bf16 bits, 1 = float32.              */
+int oracle_ep_combine(int W, const int64_t *tok_off, int k, int E, int H,
+                      const int32_t *topk_idx, const float *topk_w, const uint16_t *y,
+                      void *out, int out_dtype)
+{
+    if (W < 1 || k < 1 || E < 1 || E % W != 0 || H < 1 || tok_off[0] != 0 ||
+        (out_dtype != 0 && out_dtype != 1))
+        return ORACLE_ERR_INVALID_ARG;
+    const int El = E / W;
+    const int64_t T = tok_off[W];
+    for (int64_t i = 0; i < T * k; ++i)
+        if (topk_idx[i] < 0 || topk_idx[i] >= E)
+            return ORACLE_ERR_BAD_INDEX;
+    /* row of each pair: the same walk as the dispatch */
+    int64_t *row_of = (int64_t *)malloc(sizeof(int64_t) * (size_t)(T * k > 0 ? T * k : 1));
+    if (row_of == NULL)
+        return ORACLE_ERR_INVALID_ARG;
+    int64_t row = 0;
+    for (int d = 0; d < W; ++d)
+        for (int el = 0; el < El; ++el)
+            for (int s = 0; s < W; ++s)
+                for (int64_t t = tok_off[s]; t < tok_off[s + 1]; ++t)
+                    for (int j = 0; j < k; ++j)
+                        if (topk_idx[t * k + j] == d * El + el)
+                            row_of[t * k + j] = row++;
+    for (int64_t t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                const int64_t i = t * k + j;
+                acc = fmaf(topk_w[i], bf16_to_f32(y[row_of[i] * H + h]), acc);
+            }
+            if (out_dtype == 0)
+                ((uint16_t *)out)[t * H + h] = oracle_f32_to_bf16(acc);
+            else
+                ((float *)out)[t * H + h] = acc;
+        }
+    free(row_of);
     return ORACLE_OK;
 }
 

@@ -12,6 +12,7 @@ import test_oracle_layout as tl
 import test_oracle_bf16 as tb
 import test_oracle_backward as tbw
 import test_oracle_coalesced as tco
+import test_oracle_ep as tep
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "moe_oracle.c")
@@ -51,6 +52,15 @@ MUTANTS = {
     # coalesced combine: the token adds its row once per slot, not once per row
     "post_duplicates": ("if (first)\n                    acc = acc + bf16_to_f32(partial",
                         "if (1)\n                    acc = acc + bf16_to_f32(partial"),
+    # expert parallelism: a receiver takes its sources in reverse order
+    "ep_source_order": ("            for (int s = 0; s < W; ++s) {\n                int32_t cnt = 0;",
+                        "            for (int s = W - 1; s >= 0; --s) {\n                int32_t cnt = 0;"),
+    # expert parallelism: counts filed [source][receiver] instead of [receiver][source]
+    "ep_counts_index": ("recv_counts[((int64_t)d * W + s) * El + el] = cnt;",
+                        "recv_counts[((int64_t)s * W + d) * El + el] = cnt;"),
+    # expert parallelism: the return path sums a token's slots in reverse order
+    "ep_combine_order": ("            for (int j = 0; j < k; ++j) {\n                const int64_t i = t * k + j;\n                acc = fmaf(topk_w[i], bf16_to_f32(y[row_of[i] * H + h]), acc);",
+                         "            for (int j = k - 1; j >= 0; --j) {\n                const int64_t i = t * k + j;\n                acc = fmaf(topk_w[i], bf16_to_f32(y[row_of[i] * H + h]), acc);"),
     # bf16: ties rounded up instead of to even
     "bf16_ties": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (lower >= 0x8000u)"),
 }
@@ -77,7 +87,10 @@ def _pins():
              tco.test_coalesced_hand_worked,
              lambda: tco.test_coalesced_layout_matches_brute_force(*tco.CASES[7]),
              lambda: tco.test_coalesced_combine_integer_payload_is_exact(1, 64, 8, 32, 4),
-             lambda: tco.test_coalesced_combine_on_one_rank_is_plain_combine(40, 8, 16)]
+             lambda: tco.test_coalesced_combine_on_one_rank_is_plain_combine(40, 8, 16),
+             lambda: tep.test_receive_buffers_are_the_stable_order_of_all_tokens(tep.CASES[2]),
+             lambda: tep.test_counts_are_per_source_bincounts(tep.CASES[1]),
+             tep.test_hand_worked_two_ranks, tep.test_combine_accumulates_in_slot_order]
     return pins
 
 
