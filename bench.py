@@ -593,10 +593,16 @@ class StepBench:
         self.flush_r.view(torch.int64).sum()
 
     def launches_per_step(self):
-        # layout, dispatch, combine; the coalesced step adds the coalesced
-        # layout (a second launch when k does not divide 32)
+        # layout, dispatch, combine (layout and dispatch are one kernel when
+        # moe_layout_dispatch takes its single-kernel form); the coalesced
+        # step adds the coalesced layout (a second launch when k does not
+        # divide 32)
         if self.coal:
             return 4 if 32 % self.k == 0 else 5
+        if self.fused_front:
+            self.front()
+            if self.m.moe_layout_last_form() == self.m.MOE_LAYOUT_FORM_FUSED:
+                return 2
         return 3
 
     def step(self, ev=None):
@@ -748,9 +754,12 @@ def run_gpu(args):
     import torch.distributed as dist
 
     rank, world, local = dist_env()
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
+    if world > 1 and not dist.is_initialized():
+        import datetime
+        dist.init_process_group("nccl", timeout=datetime.timedelta(seconds=180))
+    if world > 1 or args.ep_virtual > 1:
+        return run_gpu_ep(args, rank, world, local)
     dev = torch.device("cuda", local)
 
     import combine_layout_moe_gb300 as m
@@ -863,6 +872,105 @@ def run_gpu(args):
         line["cpu_baseline"] = cpu_baseline(name, args.cpu_budget, wh, xh, yh)
         for nm, (wo, xo, yo) in host_inputs.items():
             per_config[nm]["oracle_1core"] = oracle_op_times(nm, xo, yo, wo)
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu_ep(args, rank, world, local):
+    """Expert parallelism across ranks.  Under torchrun (N > 1) each GPU is
+    one rank of W = N: it holds T tokens of the workload (drawn with seed
+    seed + rank) and E / W of the experts, and a step is layout (R = W) ->
+    dispatch -> the counts all-to-all and the rows' all-to-all-v over NCCL ->
+    the receiver's reorder -> identity experts -> the reverse reorder and
+    all-to-all-v -> combine.  With --ep-virtual W on one GPU the W ranks run
+    in one process and the exchange is a device copy of each segment.  The
+    timed step brackets the whole of it with CUDA events on the current
+    stream (the host reads the split sizes back twice per step, as any
+    all-to-all-v must); value = W x T tokens over the MAX over ranks."""
+    import torch
+    import combine_layout_moe_gb300 as m
+    from combine_layout_moe_gb300 import ep
+    from workloads.gen import make_workload, device_inputs
+
+    dev = torch.device("cuda", local)
+    name = args.config
+    virtual = world == 1
+    W = args.ep_virtual if virtual else world
+    err = m.new_error_word(dev)
+    ops = ep.LibraryOps(err)
+    mine = range(W) if virtual else [rank]
+    ws_, xs, idxs, wts = [], [], [], []
+    for r in mine:
+        w = make_workload(name, seed=args.seed + r)
+        x, _ = device_inputs(w, dev)
+        ws_.append(w)
+        xs.append(x)
+        idxs.append(torch.from_numpy(w.topk_idx).to(dev))
+        wts.append(torch.from_numpy(w.topk_w).to(dev))
+    T, H, k, E = ws_[0].T, ws_[0].H, ws_[0].k, ws_[0].E
+    if E % W:
+        raise SystemExit(f"{name}: E = {E} experts do not divide over {W} ranks")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    epl = None if virtual else ep.ExpertParallel(E, ops=ops)
+
+    def step():
+        if virtual:
+            return ep.virtual_step(xs, idxs, wts, E, ops=ops)[2]
+        recv, offs, handle = epl.dispatch(xs[0], idxs[0])
+        return [epl.combine(recv, handle, wts[0])]
+
+    for _ in range(args.warmup):
+        outs = step()
+    torch.cuda.synchronize()
+    bits = m.moe_read_error(err)
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x} during warm-up")
+    # identity experts and weights summing to one: each rank's tokens come back
+    for x, o in zip(xs, outs):
+        nz = x != 0
+        if not torch.equal(o[nz].view(torch.int16), x[nz].view(torch.int16)):
+            raise RuntimeError("expert-parallel round trip did not return x")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    nv = NvmlClocks(gpu_smi_id(torch, dev))
+    barrier()
+    torch.cuda.synchronize()
+    with nv:
+        for a, b in ev:
+            flush.fill_(0)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = allreduce_max(sum(a.elapsed_time(b) for a, b in ev))
+    ms = total_ms / args.steps
+    if rank != 0:
+        return
+    tokens = W * T
+    peak, peak_kind = measured_peak_gbs()
+    line = {
+        "metric": METRIC, "value": tokens / (ms / 1000.0), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{name} T={T} per rank H={H} k={k} E={E}",
+                   "parallelism": (f"ep{W} virtual ranks on one GPU (exchange by device copy)"
+                                   if virtual else f"ep{W}: experts over {W} GPUs, NCCL "
+                                                   "all-to-all-v"),
+                   "tokens_per_step": tokens,
+                   "l2": "2xL2 written before each step, outside the events"},
+        "step": "layout (R = W) -> dispatch -> counts all-to-all -> rows all-to-all-v -> "
+                "receiver reorder -> identity experts -> reverse reorder -> rows all-to-all-v "
+                "-> combine",
+        "roofline": None,
+        "roofline_note": f"the step includes the exchange and two host readbacks of split "
+                         f"sizes; the local kernels' fractions of HBM peak ({peak_kind} "
+                         f"{peak} GB/s) are in the single-GPU line",
+        "gpu_launches": (5 if not virtual else 5 * W) * args.steps,  # layout, dispatch, 2 reorders, combine
+        "clocks": nv.summary(),
+    }
     print(json.dumps(line), flush=True)
 
 
@@ -1111,6 +1219,9 @@ def main(argv=None):
                    help="comma-separated workloads timed after the headline, each through "
                         "the same loop, reported in the line's per_config block")
     p.add_argument("--no-per-config", action="store_true")
+    p.add_argument("--ep-virtual", type=int, default=1,
+                   help="on one GPU: time expert parallelism over W virtual ranks (the "
+                        "exchange done by device copies) instead of the single-GPU step")
     p.add_argument("--variant", choices=["plain", "coalesced"], default="plain",
                    help="plain: the hot path; coalesced: the rank-coalesced path")
     p.add_argument("--table", action="store_true",

@@ -26,6 +26,7 @@ MOE_ERRBIT_LAUNCH = 0x10
 MOE_LAYOUT_FORM_NONE, MOE_LAYOUT_FORM_SINGLE, MOE_LAYOUT_FORM_CLUSTER, \
     MOE_LAYOUT_FORM_COOPERATIVE, MOE_LAYOUT_FORM_FUSED = range(5)
 MOE_SYNC_WORD, MOE_SYNC_SENTINEL, MOE_SYNC_BATCH, MOE_SYNC_BARRIER = range(4)
+MOE_EP_TO_EXPERT, MOE_EP_TO_SOURCE = 0, 1
 MOE_MAX_EXPERTS = 1024
 
 # Every symbol the header declares, with its ctypes signature.
@@ -44,6 +45,7 @@ SIGNATURES = {
     "moe_layout_noalloc": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_sync_words": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
     "moe_layout_last_form": ([], ctypes.c_int),
+    "moe_ep_reorder": ([_I, _I, _I, _P, _I, _P, _P, _I, _P, _U32P, _P], ctypes.c_int),
     "moe_combine_backward": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_dispatch_backward": ([_I, _I, _I, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_layout_coalesced": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P],
@@ -514,3 +516,29 @@ __all__ = [
     "moe_combine_coalesced",
     "moe_dispatch_combine_flagged", "LIB_PATH", "SIGNATURES",
 ]
+
+
+def moe_ep_reorder(src: torch.Tensor, recv_counts: torch.Tensor, *, to_source: bool = False,
+                   out: Optional[torch.Tensor] = None,
+                   local_expert_offsets: Optional[torch.Tensor] = None,
+                   err_word: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Source-major received rows -> expert-major (to_source False), or back
+    (True); recv_counts is the [W, El] int32 device matrix of rows each source
+    sent for each local expert (see moe_ep.h)."""
+    if recv_counts.dim() != 2:
+        raise ValueError("recv_counts must be [W, El]")
+    W, El = recv_counts.shape
+    rows, H = src.shape
+    _want(src, "src", torch.bfloat16)
+    _want(recv_counts, "recv_counts", torch.int32)
+    if out is None:
+        out = torch.empty_like(src)
+    _want(out, "out", torch.bfloat16, (rows, H))
+    if local_expert_offsets is not None:
+        _want(local_expert_offsets, "local_expert_offsets", torch.int32, (El + 1,))
+    _check(_lib.moe_ep_reorder(W, El, H, _ptr(recv_counts), rows, _ptr(src), _ptr(out),
+                               MOE_EP_TO_SOURCE if to_source else MOE_EP_TO_EXPERT,
+                               _ptr(local_expert_offsets), _ptr(err_word), _stream(stream)),
+           "moe_ep_reorder")
+    return out

@@ -55,6 +55,29 @@ __host__ __device__ constexpr size_t fused_payload_offset(int E)
     return (256 + sizeof(int32_t) * (2 * (size_t)E + 2 * FUSED_MAX_OWN + 4) + 127) / 128 * 128;
 }
 
+// Phase timestamps for tuning builds (-DMOE_TRACE): CTA 0 stores %globaltimer
+// at phase boundaries into the 64-bit words that follow the error word; word
+// 14 gets the latest CTA start and word 15 the latest CTA end.
+#ifdef MOE_TRACE
+#define FUSED_TRACE(n)                                                                 \
+    do {                                                                               \
+        if (blockIdx.x == 0 && threadIdx.x == 0 && err_word)                            \
+            reinterpret_cast<unsigned long long *>(err_word)[8 + (n)] = global_ns();   \
+    } while (0)
+#define FUSED_TRACE_MAX(n)                                                                      \
+    do {                                                                                        \
+        if (threadIdx.x == 0 && err_word)                                                       \
+            atomicMax(reinterpret_cast<unsigned long long *>(err_word) + 8 + (n), global_ns()); \
+    } while (0)
+#else
+#define FUSED_TRACE(n) \
+    do {               \
+    } while (0)
+#define FUSED_TRACE_MAX(n) \
+    do {                   \
+    } while (0)
+#endif
+
 __global__ void __launch_bounds__(FUSED_THREADS, 1)
     layout_dispatch_fused_kernel(const int32_t *__restrict__ idx, const uint8_t *__restrict__ x,
                                  int T, int k, int E, int R, int64_t rowbytes, int CH, int nch,
@@ -81,8 +104,22 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     const int64_t t_lo = u_lo / nch, t_hi = (u_hi - 1) / nch;
     const int64_t P0 = t_lo * k, P1 = (t_hi + 1) * k;
     const int p = (int)(P1 - P0);                  // <= FUSED_MAX_OWN (checked on the host)
-    const int64_t t_own = (u_lo + nch - 1) / nch;  // first token whose chunk 0 is here
+    FUSED_TRACE(0);
+    FUSED_TRACE_MAX(6);
 
+    wait_prior_grid();
+    allow_next_grid();
+    // the first batch of ids is requested before anything else: their
+    // latency is the head of the critical path
+    const bool vec = (reinterpret_cast<uintptr_t>(idx) & 15) == 0;
+    const int64_t nv = vec ? N / 4 : 0;
+    const int4 *iv = reinterpret_cast<const int4 *>(idx);
+    int4 v0[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t q = tid + (int64_t)u * nthr;
+        v0[u] = q < nv ? ld_nc_v4_s32(iv + q) : make_int4(0, 0, 0, 0);
+    }
     for (int i = tid; i < 2 * E; i += nthr)
         pre[i] = 0;
     if (tid < 4)
@@ -93,18 +130,21 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         mbar_fence_init();
     }
     __syncthreads();
-    wait_prior_grid();
-    allow_next_grid();
 
     // 1. the CTA's share of x, one bulk copy per unit
-    if (tid < Uc) {
-        const int64_t u = u_lo + tid, t = u / nch;
-        const int c = (int)(u - t * nch);
-        const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
-        mbar_arrive_expect_tx(bars + 8u * tid, cb);
-        bulk_g2s(payload + (uint32_t)tid * CH, x + t * rowbytes + (int64_t)c * CH, cb,
-                 bars + 8u * tid);
-    }
+    auto load_x = [&]() {
+        if (tid < Uc) {
+            const int64_t u = u_lo + tid, t = u / nch;
+            const int c = (int)(u - t * nch);
+            const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)c * CH);
+            mbar_arrive_expect_tx(bars + 8u * tid, cb);
+            bulk_g2s(payload + (uint32_t)tid * CH, x + t * rowbytes + (int64_t)c * CH, cb,
+                     bars + 8u * tid);
+        }
+    };
+#ifdef MOE_FUSED_X_FIRST
+    load_x();
+#endif
 
     // 2. the whole batch's histogram, split at this CTA's first pair P0
     bool bad = false;
@@ -120,15 +160,13 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         if (mine)
             own[i - P0] = e;
     };
-    if ((reinterpret_cast<uintptr_t>(idx) & 15) == 0) {
-        const int64_t nv = N / 4;
-        const int4 *iv = reinterpret_cast<const int4 *>(idx);
+    if (vec) {
         for (int64_t q0 = tid; q0 < nv; q0 += (int64_t)nthr * 4) {
             int4 v[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int64_t q = q0 + (int64_t)u * nthr;
-                v[u] = q < nv ? ld_nc_v4_s32(iv + q) : make_int4(0, 0, 0, 0);
+                v[u] = q0 == tid ? v0[u] : q < nv ? ld_nc_v4_s32(iv + q) : make_int4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -161,11 +199,19 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     }
     if (bad)
         flags[0] = 1;
+#ifndef MOE_FUSED_X_FIRST
+    // issued once the ids are in: the ids then meet an idle memory system,
+    // and x (at most ~200 KB per SM) still lands before the slots are known
+    load_x();
+#endif
     __syncthreads();
+    FUSED_TRACE(1);
 
-    // 3a. exclusive scan of the totals over experts by warp 0: each lane sums
-    //     a run of ceil(E/32) experts, one warp scan, each lane writes its
-    //     run's offsets (post) and cursors (pre: offset + pairs before P0)
+    // 3. warp 0: exclusive scan of the totals over experts.  Each lane sums
+    //    a run of ceil(E/32) experts, one warp scan, each lane writes its
+    //    run's offsets (post) and cursors (pre: offset + pairs before P0).
+    //    Meanwhile the other warps rank each pair of this CTA's tokens among
+    //    the earlier such pairs of its expert (sl: the rank, or -1).
     if (tid < 32) {
         const int lane = tid;
         const int per = (E + 31) / 32;
@@ -194,8 +240,21 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         }
         if (lane == 31)
             flags[1] = incl;
+    } else {
+        for (int q = tid - 32; q < p; q += nthr - 32) {
+            const int e = own[q];
+            int32_t c = -1;
+            if (e >= 0) {
+                c = 0;
+#pragma unroll 8
+                for (int q2 = 0; q2 < q; ++q2)  // independent loads, eight in flight
+                    c += own[q2] == e;
+            }
+            sl[q] = c;
+        }
     }
     __syncthreads();
+    FUSED_TRACE(2);
     if (blockIdx.x == 0) {
         const int32_t total = flags[1];
         if (tid == 0)
@@ -204,35 +263,26 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         for (int r = tid; r <= R; r += nthr)
             rank_offsets[r] = r == R ? total : post[r * El];
     }
+    FUSED_TRACE(3);
 
-    // 3b. slots of the pairs of this CTA's tokens; the CTA holding a token's
-    //     first chunk writes its slot_of and src_of entries
-    for (int q = tid; q < p; q += nthr) {
-        const int e = own[q];
-        int32_t s = -1;
-        if (e >= 0) {
-            int c = 0;
-            for (int q2 = 0; q2 < q; ++q2)
-                c += own[q2] == e;
-            s = pre[e] + c;
-        }
-        sl[q] = s;
-        const int64_t i = P0 + q;
-        if (i / k >= t_own) {
-            slot_of[i] = s;
-            if (s >= 0)
-                src_of[s] = (int32_t)i;
-        }
-    }
-    __syncthreads();
-
-    // 4. every landed unit to its k slots
+    // 4. every landed unit to its k slots: slot = cursor of the expert + the
+    //    pair's rank among this CTA's pairs of that expert.  The task of a
+    //    token's first chunk also writes the pair's slot_of and src_of entries
+    //    (each token's first chunk lies in exactly one CTA).
     bool timed_out = false;
     for (int task = tid; task < Uc * k; task += nthr) {
         const int q = task / k, j = task - q * k;
         const int64_t u = u_lo + q, t = u / nch;
         const int c = (int)(u - t * nch);
-        const int32_t s = sl[(t - t_lo) * k + j];
+        const int qo = (int)(t - t_lo) * k + j;
+        const int e = own[qo];
+        const int32_t s = e >= 0 ? pre[e] + sl[qo] : -1;
+        if (c == 0) {
+            const int64_t i = t * k + j;
+            slot_of[i] = s;
+            if (s >= 0)
+                src_of[s] = (int32_t)i;
+        }
         if ((unsigned)s >= (unsigned)N)
             continue;  // an id out of range: reported below
         if (!mbar_wait(bars + 8u * q, 0)) {
@@ -246,8 +296,11 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     }
     if (timed_out)
         flags[2] = 1;
+    FUSED_TRACE(4);
     bulk_wait_all();
     __syncthreads();
+    FUSED_TRACE(5);
+    FUSED_TRACE_MAX(7);
     if (flags[2]) {
         // a load that did not land in time: report it, and let every issued
         // load land (again bounded) before the CTA's shared memory goes away
@@ -260,22 +313,53 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         report(err_word, MOE_ERRBIT_BAD_INDEX);
 }
 
-bool layout_dispatch_fused_fits(int T, int H, int k, int E)
+// How a batch is cut into units: rows split into nch chunks of CH bytes (a
+// multiple of 16), the units spread over G CTAs, at most umax per CTA.  Rows
+// are split further while that keeps at most FUSED_TARGET_UNITS units per CTA
+// and chunks of at least FUSED_MIN_CHUNK bytes: finer units even out the
+// CTAs' shares (1024 rows of 14 KB over 152 SMs is 6 or 7 rows each, 16 %
+// apart; halves of rows are 13 or 14, 7 % apart).
+struct FusedPlan {
+    bool ok;
+    int CH, nch, G, umax;
+    int64_t units;
+};
+
+constexpr int FUSED_TARGET_UNITS = 24;
+constexpr int FUSED_MIN_CHUNK = 2048;
+
+static FusedPlan fused_plan(int T, int H, int k, int E)
 {
+    FusedPlan p{false, 0, 0, 0, 0, 0};
     const int64_t N = (int64_t)T * k;
     if (T < 1 || N > FUSED_MAX_PAIRS || k > 32 || E > MOE_MAX_EXPERTS)
-        return false;
+        return p;
     const int64_t rowbytes = 2 * (int64_t)H;
-    const int CH = rowbytes < FUSED_CHUNK ? (int)rowbytes : FUSED_CHUNK;
-    const int64_t nch = (rowbytes + CH - 1) / CH;
-    const int64_t units = (int64_t)T * nch;
-    const int64_t G = units < sm_count() ? units : sm_count();
-    const int64_t umax = (units + G - 1) / G;
-    if (umax > FUSED_MAX_UNITS || (size_t)umax * CH > FUSED_PAYLOAD_MAX)
-        return false;
+    const int sms = sm_count();
+    auto cut = [&](int64_t want, FusedPlan &q) {
+        const int64_t ch = ((rowbytes + want - 1) / want + 15) / 16 * 16;
+        q.CH = (int)(ch < FUSED_CHUNK ? ch : FUSED_CHUNK);
+        q.nch = (int)((rowbytes + q.CH - 1) / q.CH);
+        q.units = (int64_t)T * q.nch;
+        q.G = (int)(q.units < sms ? q.units : sms);
+        q.umax = (int)((q.units + q.G - 1) / q.G);
+    };
+    cut((rowbytes + FUSED_CHUNK - 1) / FUSED_CHUNK, p);
+    for (;;) {
+        FusedPlan q = p;
+        cut(2 * (int64_t)p.nch, q);
+        if (q.nch <= p.nch || q.CH < FUSED_MIN_CHUNK || q.umax > FUSED_TARGET_UNITS)
+            break;
+        p = q;
+    }
+    if (p.umax > FUSED_MAX_UNITS || (size_t)p.umax * p.CH > FUSED_PAYLOAD_MAX)
+        return p;
     // a CTA's units span at most ceil(umax / nch) + 1 tokens
-    return ((umax + nch - 1) / nch + 1) * k <= FUSED_MAX_OWN;
+    p.ok = ((p.umax + p.nch - 1) / p.nch + 1) * (int64_t)k <= FUSED_MAX_OWN;
+    return p;
 }
+
+bool layout_dispatch_fused_fits(int T, int H, int k, int E) { return fused_plan(T, H, k, E).ok; }
 
 cudaError_t launch_layout_dispatch_fused(int T, int H, int k, int E, int R,
                                          const int32_t *topk_idx, const void *x,
@@ -284,21 +368,18 @@ cudaError_t launch_layout_dispatch_fused(int T, int H, int k, int E, int R,
                                          int32_t *src_of, void *recv, uint32_t *err_word,
                                          cudaStream_t stream)
 {
-    const int64_t rowbytes = 2 * (int64_t)H;
-    const int CH = rowbytes < FUSED_CHUNK ? (int)rowbytes : FUSED_CHUNK;
-    const int nch = (int)((rowbytes + CH - 1) / CH);
-    const int64_t units = (int64_t)T * nch;
-    const int64_t G = units < sm_count() ? units : sm_count();
-    const int64_t umax = (units + G - 1) / G;
-    const size_t smem = fused_payload_offset(E) + (size_t)umax * CH;
+    const FusedPlan p = fused_plan(T, H, k, E);
+    if (!p.ok)
+        return cudaErrorInvalidValue;
+    const size_t smem = fused_payload_offset(E) + (size_t)p.umax * p.CH;
     cudaError_t e = cudaFuncSetAttribute(layout_dispatch_fused_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    e = launch_pdl(layout_dispatch_fused_kernel, dim3((unsigned)G), dim3(FUSED_THREADS), smem,
-                   stream, topk_idx, static_cast<const uint8_t *>(x), T, k, E, R, rowbytes, CH,
-                   nch, units, expert_counts, expert_offsets, rank_offsets, slot_of, src_of,
-                   static_cast<uint8_t *>(recv), err_word);
+    e = launch_pdl(layout_dispatch_fused_kernel, dim3((unsigned)p.G), dim3(FUSED_THREADS), smem,
+                   stream, topk_idx, static_cast<const uint8_t *>(x), T, k, E, R,
+                   2 * (int64_t)H, p.CH, p.nch, p.units, expert_counts, expert_offsets,
+                   rank_offsets, slot_of, src_of, static_cast<uint8_t *>(recv), err_word);
     if (e == cudaSuccess)
         note_layout_form(MOE_LAYOUT_FORM_FUSED);
     return e;

@@ -419,6 +419,47 @@ MOE_API moe_status moe_dispatch_combine_flagged(int T, int H, int k, const void 
                                         cudaStream_t stream);
 
 /*
+ * moe_ep_reorder -- the receiver's reorder of expert-parallel dispatch across
+ * real ranks, and its inverse on the combine's return path.
+ *
+ * UBEP, section 2.3 and Figure 2 (the receive region is partitioned by source
+ * rank and expert; in Phase 5 the receiver computes offsets from every
+ * source's per-expert counts and reorders the tokens contiguously per
+ * expert) and section 4 (receive address space partitioned in advance);
+ * StrataCL, Appendix D (the same counts return the rows on the combine path).
+ *
+ * With experts spread over W ranks (El = E / W local experts each), every
+ * rank runs moe_layout with R = W over its own tokens and moe_dispatch; the
+ * rank segments of its receive buffer are its sends.  After the exchange
+ * (an all-to-all of those segments) a receiver holds the rows source by
+ * source -- for source s, its rows for local expert 0, 1, ... in s's (token,
+ * slot) order.  This call places them expert-major: for local expert el the
+ * rows of source 0, then 1, ..., each in its source's order.
+ *
+ *   recv_counts  [W, El] int32 device: rows source s sent for local expert
+ *                el (the El counts of this rank's experts in s's
+ *                expert_counts)
+ *   rows         the sum of recv_counts; src and dst hold `rows` rows
+ *   src, dst     [rows, H] bf16, 16-byte aligned, not the same buffer
+ *   direction    MOE_EP_TO_EXPERT: dst[expert-major(q)] = src[q] (dispatch);
+ *                MOE_EP_TO_SOURCE: dst[q] = src[expert-major(q)] (the return
+ *                path: expert outputs back to source-major order)
+ *   local_expert_offsets  [El+1] int32 device out, may be NULL: first row of
+ *                each local expert in the expert-major order; [El] = rows
+ *
+ * Counts that are negative or do not add up to `rows` set
+ * MOE_ERRBIT_BAD_INDEX and copy nothing.  W * El <= MOE_MAX_EXPERTS
+ * (larger: MOE_ERR_UNSUPPORTED); H % 8 == 0.
+ */
+#define MOE_EP_TO_EXPERT 0
+#define MOE_EP_TO_SOURCE 1
+
+MOE_API moe_status moe_ep_reorder(int W, int El, int H, const int32_t *recv_counts, int rows,
+                                  const void *src, void *dst, int direction,
+                                  int32_t *local_expert_offsets, uint32_t *err_word,
+                                  cudaStream_t stream);
+
+/*
  * moe_layout_noalloc -- moe_layout for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a deployment convenience.
  *

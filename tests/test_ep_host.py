@@ -1,0 +1,162 @@
+"""Expert parallelism across real ranks, host side, on CPU: two (and three)
+gloo ranks run the exchange of combine_layout_moe_gb300.ep -- the counts
+all-to-all, the split sizes read back to the host, the all-to-all-v of the
+rows there and back -- with the local steps (layout, dispatch, reorder,
+combine) replaced by CPU stand-ins.  The receive buffers, expert offsets and
+combined outputs must equal the oracle's expert-parallel dispatch and combine
+of all ranks' tokens.
+
+The stand-ins: layout, dispatch and combine are the oracle's single-rank
+functions; the reorder is written out below from its contract (source-major
+segments -> expert-major).  The CUDA kernels behind the same phases are
+checked against the oracle on the GPU (tests/test_gpu_ep.py)."""
+import os
+import socket
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import oracle
+from workloads.gen import random_case, expert_output
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+class CpuOps:
+    """CPU stand-ins for the library's local steps (test scaffolding)."""
+
+    def layout(self, topk_idx, E, W):
+        c, o, ro, so, src = oracle.layout(topk_idx.numpy(), E, W)
+        t = torch.from_numpy
+        return SimpleNamespace(expert_counts=t(c), expert_offsets=t(o), rank_offsets=t(ro),
+                               slot_of=t(so), src_of=t(src))
+
+    def dispatch(self, x, slot_of):
+        return _bf16(oracle.dispatch(_bits(x), slot_of.numpy()))
+
+    def reorder(self, src, recv_counts, to_source, with_offsets):
+        cnt = recv_counts.numpy().astype(np.int64)
+        W, El = cnt.shape
+        s_start = np.concatenate([[0], np.cumsum(cnt.reshape(-1))])[:-1].reshape(W, El)
+        e_start = np.concatenate([[0], np.cumsum(cnt.T.reshape(-1))])[:-1].reshape(El, W).T
+        perm = np.empty(int(cnt.sum()), np.int64)       # source-major row -> expert-major row
+        for s in range(W):
+            for el in range(El):
+                n = cnt[s, el]
+                perm[s_start[s, el]:s_start[s, el] + n] = e_start[s, el] + np.arange(n)
+        a = _bits(src)
+        out = np.empty_like(a)
+        if to_source:
+            out[:] = a[perm]
+        else:
+            out[perm] = a
+        offs = None
+        if with_offsets:
+            offs = torch.from_numpy(np.append(e_start[0], cnt.sum()).astype(np.int32))
+        return _bf16(out), offs
+
+    def combine(self, y, slot_of, topk_w):
+        return _bf16(oracle.combine(_bits(y), slot_of.numpy(), topk_w.numpy(), "bf16"))
+
+
+def _inputs(W, T_per, H, k, E):
+    return [random_case(500 + s, T_per[s], H, k, E, W) for s in range(W)]
+
+
+def _rank_main(rank, W, port, T_per, H, k, E, q):
+    import torch.distributed as dist
+    from combine_layout_moe_gb300 import ep
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=W)
+    try:
+        ins = _inputs(W, T_per, H, k, E)
+        me = ins[rank]
+        epl = ep.ExpertParallel(E, ops=CpuOps())
+        recv, offs, handle = epl.dispatch(_bf16(me.x), torch.from_numpy(me.topk_idx))
+        # an expert that is not the identity: each receiver's own rows
+        y = _bf16(expert_output(recv.shape[0], H, seed=900 + rank))
+        out = epl.combine(y, handle, torch.from_numpy(me.topk_w))
+        q.put((rank, _bits(recv), offs.numpy(), _bits(out), handle[1].recv_splits,
+               handle[0].send_splits))
+    except Exception as e:  # reported to the parent, which fails the test
+        q.put((rank, repr(e)))
+    finally:
+        dist.destroy_process_group()
+
+
+def _port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+@pytest.mark.parametrize("W,T_per,H,k,E", [(2, [37, 23], 16, 2, 4), (2, [40, 0], 8, 3, 8),
+                                           (3, [11, 29, 5], 24, 8, 6)])
+def test_exchange_over_gloo_matches_oracle(W, T_per, H, k, E):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _port()
+    procs = [ctx.Process(target=_rank_main, args=(r, W, port, T_per, H, k, E, q))
+             for r in range(W)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(W):
+        item = q.get(timeout=120)
+        res[item[0]] = item
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(W):
+        assert len(res[r]) > 2, res[r][1]
+    ins = _inputs(W, T_per, H, k, E)
+    counts, recv, _ = oracle.ep_dispatch([w.topk_idx for w in ins], [w.x for w in ins], E)
+    El = E // W
+    ys = [expert_output(len(recv[d]), H, seed=900 + d) for d in range(W)]
+    outs = oracle.ep_combine([w.topk_idx for w in ins], [w.topk_w for w in ins], ys, E)
+    for d in range(W):
+        _, g_recv, g_offs, g_out, recv_splits, send_splits = res[d]
+        assert np.array_equal(g_recv.reshape(recv[d].shape), recv[d])
+        # local expert offsets: the expert-major start of each local expert
+        want = np.concatenate([[0], np.cumsum(counts[d].sum(axis=0))])
+        assert np.array_equal(g_offs, want)
+        assert recv_splits == counts[d].sum(axis=1).tolist()
+        assert send_splits == [int(counts[dd, d].sum()) for dd in range(W)]
+        assert np.array_equal(g_out.reshape(outs[d].shape), outs[d])
+        assert El >= 1
+
+
+def test_virtual_step_on_cpu_stand_ins_matches_oracle():
+    """The single-process driver (the exchange done by copies) with the same
+    stand-ins: the phases compose to the oracle's result."""
+    from combine_layout_moe_gb300 import ep
+    W, H, k, E = 4, 8, 2, 8
+    ins = _inputs(W, [9, 0, 14, 3], H, k, E)
+    ys = {}
+
+    def expert(recv, offs):
+        d = len(ys)
+        ys[d] = expert_output(recv.shape[0], H, seed=700 + d)
+        return _bf16(ys[d])
+
+    recv, offs, outs = ep.virtual_step([_bf16(w.x) for w in ins],
+                                       [torch.from_numpy(w.topk_idx) for w in ins],
+                                       [torch.from_numpy(w.topk_w) for w in ins], E,
+                                       expert=expert, ops=CpuOps())
+    _, o_recv, _ = oracle.ep_dispatch([w.topk_idx for w in ins], [w.x for w in ins], E)
+    o_out = oracle.ep_combine([w.topk_idx for w in ins], [w.topk_w for w in ins],
+                              [ys[d] for d in range(W)], E)
+    for d in range(W):
+        assert np.array_equal(_bits(recv[d]).reshape(o_recv[d].shape), o_recv[d])
+        assert np.array_equal(_bits(outs[d]).reshape(o_out[d].shape), o_out[d])
