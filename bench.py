@@ -1202,6 +1202,110 @@ def run_table(args):
         torch.cuda.empty_cache()
 
 
+def run_profile_op(args):
+    """One entry point on one workload, for an ncu capture: args.warmup
+    launches, then args.steps launches, each after a write of 2xL2 and a read
+    of 4xL2 and bracketed by CUDA events; prints the median.  Only the buffers
+    that entry point needs are allocated.  --shape T,H,k,E,R replaces the
+    workload by a uniform random routing of that shape."""
+    import torch
+    import combine_layout_moe_gb300 as m
+    from workloads.gen import make_workload, random_case, device_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.shape:
+        T, H, k, E, R = (int(v) for v in args.shape.split(","))
+        w = random_case(args.seed, T, H, k, E, R)
+        name = f"random T={T} H={H} k={k} E={E} R={R}"
+    else:
+        w = make_workload(args.config, seed=args.seed)
+        T, H, k, E, R = w.T, w.H, w.k, w.E, w.R
+        name = f"{args.config} T={T} H={H} k={k} E={E} R={R}"
+    N = T * k
+    x, y = device_inputs(w, dev)
+    idx = torch.from_numpy(w.topk_idx).to(dev)
+    wt = torch.from_numpy(w.topk_w).to(dev)
+    err = m.new_error_word(dev)
+    ws = m.new_workspace(m.moe_layout_workspace_bytes(T, k, E), dev)
+    lay = m.moe_layout(idx, E, R, workspace=ws, err_word=err)
+    kw = dict(err_word=err)
+    op = args.profile_op
+    if op in ("layout_coalesced", "dispatch_coalesced", "combine_coalesced"):
+        wsc = m.new_workspace(m.moe_layout_workspace_bytes(T, k, R), dev)
+        co = m.moe_layout_coalesced(idx, lay.slot_of, E, R, workspace=wsc, err_word=err)
+        rows = T * min(k, R)
+    if op == "layout":
+        fn = lambda: m.moe_layout(idx, E, R, workspace=ws, out=lay, **kw)  # noqa: E731
+    elif op == "layout_dispatch":
+        recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: m.moe_layout_dispatch(x, idx, E, R, workspace=ws, out=lay, recv=recv,  # noqa: E731
+                                           **kw)
+    elif op == "dispatch":
+        recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: m.moe_dispatch(x, lay.slot_of, recv=recv, **kw)  # noqa: E731
+    elif op == "dispatch_fp8":
+        rq = torch.empty((N, H), dtype=torch.uint8, device=dev)
+        rs = torch.empty((N, H // 128), dtype=torch.float32, device=dev)
+        fn = lambda: m.moe_dispatch_quant(x, lay.slot_of, recv_q=rq, recv_scales=rs, **kw)  # noqa: E731
+    elif op == "combine":
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: m.moe_combine(y, lay.slot_of, wt, out=out, **kw)  # noqa: E731
+    elif op == "combine_backward":
+        dout = torch.empty((T, H), dtype=torch.bfloat16, device=dev).normal_()
+        dy = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        dw = torch.empty((T, k), dtype=torch.float32, device=dev)
+        fn = lambda: m.moe_combine_backward(dout, y, lay.slot_of, wt, dy=dy, dw=dw, **kw)  # noqa: E731
+    elif op == "dispatch_backward":
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: m.moe_dispatch_backward(y, lay.slot_of, dx=out, **kw)  # noqa: E731
+    elif op == "layout_coalesced":
+        fn = lambda: m.moe_layout_coalesced(idx, lay.slot_of, E, R, workspace=wsc, out=co, **kw)  # noqa: E731
+    elif op == "dispatch_coalesced":
+        rc = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: m.moe_dispatch_coalesced(x, co.crow, rows, recv_c=rc, **kw)  # noqa: E731
+    elif op == "combine_coalesced":
+        part = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: m.moe_combine_coalesced(y, lay.slot_of, wt, co, rows, partial=part,  # noqa: E731
+                                             out=out, **kw)
+    elif op == "ep_reorder":
+        # the receiver's reorder of R ranks' rows: the counts of a receiver
+        # that gets this workload's tokens from each of R sources, one local
+        # expert per source slice (E / R of them)
+        El = E // R
+        cnt = lay.expert_counts.view(R, El)
+        src = y[:N]
+        dst = torch.empty_like(src)
+        fn = lambda: m.moe_ep_reorder(src, cnt, out=dst, **kw)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown --profile-op {op}")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    fw = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    fr = torch.zeros(4 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # the input draw's temporaries: keep the footprint small
+    evs = []
+    for i in range(args.warmup + args.steps):
+        fw.fill_(0)
+        fr.view(torch.int64).sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        if i >= args.warmup:
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    bits = m.moe_read_error(err)
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x}")
+    us = sorted(a.elapsed_time(b) * 1000.0 for a, b in evs)
+    print(json.dumps({"profile_op": op, "workload": name, "launches": len(us),
+                      "median_us": statistics.median(us), "min_us": us[0],
+                      "layout_form": m.moe_layout_last_form()}), flush=True)
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -1219,6 +1323,13 @@ def main(argv=None):
                    help="comma-separated workloads timed after the headline, each through "
                         "the same loop, reported in the line's per_config block")
     p.add_argument("--no-per-config", action="store_true")
+    p.add_argument("--profile-op", default=None,
+                   help="time one entry point alone on --config (or --shape), for ncu "
+                        "captures: layout, layout_dispatch, dispatch, dispatch_fp8, combine, "
+                        "combine_backward, dispatch_backward, layout_coalesced, "
+                        "dispatch_coalesced, combine_coalesced, ep_reorder")
+    p.add_argument("--shape", default=None, help="with --profile-op: T,H,k,E,R of a uniform "
+                                                 "random routing instead of --config")
     p.add_argument("--ep-virtual", type=int, default=1,
                    help="on one GPU: time expert parallelism over W virtual ranks (the "
                         "exchange done by device copies) instead of the single-GPU step")
@@ -1238,7 +1349,9 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
-    if args.cpu_baseline_table:
+    if args.profile_op:
+        run_profile_op(args)
+    elif args.cpu_baseline_table:
         cpu_baseline_table(args)
     elif args.table or args.table_all or args.table_flagged:
         run_table(args)
