@@ -3,9 +3,8 @@
 //
 // UBEP, section 2.3 (Phase 2: each token goes to every expert it chose) and
 // section 4 (senders write straight into the pre-partitioned receive region);
-// RailWave, section 3.2 (payload packed without padding).  The FP8 variant
-// quantises once per token and stores the same codes to all k slots (UBEP
-// Table 3 runs DeepSeek-R1/V3.2 as W8A8).
+// RailWave, section 3.2 (payload packed without padding).  The FP8 variant is
+// in dispatch_quant.cu.
 //
 // GPU design.  The work item is one warp on one (token, row chunk): the warp
 // reads 32 x U 16-byte vectors of the token's row (U loads in flight per lane,
@@ -14,8 +13,6 @@
 // from HBM once and written k times; slot indices are read once per item by
 // lanes 0..k-1 and broadcast with shuffles.  The grid is capped at the number
 // of co-resident CTAs and strides over items.
-#include <cuda_fp8.h>
-
 #include "common.cuh"
 #include "launch.h"
 #include "tma.cuh"
@@ -161,15 +158,6 @@ __global__ void __launch_bounds__(32)
 
 constexpr int DISPATCH_THREADS = 256;
 constexpr int DISPATCH_U = 4;  // 16-byte vectors per lane per item
-// 16-lane quantisation blocks per half-warp per item (compile-time tunable;
-// the default is the shipped configuration).  Four keep 64 bytes of x in
-// flight per lane (measured on one GB300, each launch after a flush: 65536
-// tokens, H = 4096, k = 2: 227 us with 2, 204 us with 4; 8192 tokens,
-// H = 7168, k = 8: 104-105 us with either; 6 and 8 were slower at H = 7168).
-#ifndef MOE_QUANT_U
-#define MOE_QUANT_U 4
-#endif
-constexpr int QUANT_U = MOE_QUANT_U;
 
 template <int U>
 __global__ void __launch_bounds__(DISPATCH_THREADS)
@@ -207,120 +195,6 @@ __global__ void __launch_bounds__(DISPATCH_THREADS)
                 for (int u = 0; u < U; ++u)
                     if (c0 + u * 32 < C)
                         st_v4(dst + c0 + u * 32, v[u]);
-            }
-        }
-    }
-}
-
-// FP8: each half-warp owns one 128-channel block (16 lanes x 8 channels).
-// The amax is reduced with xor-shuffles inside the half-warp; scale and
-// reciprocal are each one correctly rounded fp32 division; each channel is one
-// rounded fp32 multiply followed by a saturating nearest-even E4M3 conversion.
-template <int U, bool COAL>
-__global__ void __launch_bounds__(DISPATCH_THREADS)
-    dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
-                        uint8_t *__restrict__ recv_q, float *__restrict__ recv_scales, int k,
-                        int H, int groups, int64_t items, int N, uint32_t *err_word)
-{
-    wait_prior_grid();
-    allow_next_grid();
-    const int lane = threadIdx.x & 31;
-    const int C = H >> 3;    // 16-byte vectors per row
-    const int B = H >> 7;    // 128-channel blocks per row
-    const int64_t nwarps = (int64_t)gridDim.x * (DISPATCH_THREADS / 32);
-    for (int64_t it = (int64_t)blockIdx.x * (DISPATCH_THREADS / 32) + (threadIdx.x >> 5);
-         it < items; it += nwarps) {
-        const int64_t t = it / groups;
-        const int c0 = (int)(it - t * groups) * (32 * U) + lane;
-        const uint4 *src = x + t * C;
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            v[u] = c0 + u * 32 < C ? ld_stream_v4(src + c0 + u * 32) : make_uint4(0, 0, 0, 0);
-
-        uint2 code[U];
-        float scale[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            float f[8];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                f[2 * p] = bf16lo(w[p]);
-                f[2 * p + 1] = bf16hi(w[p]);
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, o));
-            bool zero = !(amax > 0.0f);
-            float inv = 0.0f, sc = 1.0f;
-            if (!zero) {
-                inv = __fdiv_rn(448.0f, amax);
-                if (isinf(inv))
-                    zero = true;
-                else
-                    sc = __fdiv_rn(amax, 448.0f);
-            }
-            uint32_t packed[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int i = 4 * h + 2 * p;
-                    uint32_t pair;
-                    if (zero) {
-                        const uint32_t src_w = w[2 * h + p];
-                        pair = ((src_w >> 15) & 1u) << 7 | ((src_w >> 31) & 1u) << 15;
-                    } else {
-                        float2 g;
-                        g.x = __fmul_rn(f[i], inv);
-                        g.y = __fmul_rn(f[i + 1], inv);
-                        pair = __nv_cvt_float2_to_fp8x2(g, __NV_SATFINITE, __NV_E4M3);
-                    }
-                    word |= (pair & 0xffffu) << (16 * p);
-                }
-                packed[h] = word;
-            }
-            code[u] = make_uint2(packed[0], packed[1]);
-            scale[u] = sc;
-        }
-
-        const int32_t *so = slot_of + t * k;
-        for (int jb = 0; jb < k; jb += 32) {
-            const int32_t mine = jb + lane < k ? ld_nc_s32(so + jb + lane) : 0;
-            const int jn = min(32, k - jb);
-            // COAL (k <= 32): a slot whose coalesced row a lower slot of the
-            // token names stores nothing; that row is written once
-            bool first = true;
-            if (COAL) {
-                const unsigned kmask = jn >= 32 ? FULL_MASK : (1u << jn) - 1u;
-                first = (__match_any_sync(FULL_MASK, mine) & kmask & lanemask_lt()) == 0;
-            }
-            for (int q = 0; q < jn; ++q) {
-                const int32_t s = __shfl_sync(FULL_MASK, mine, q);
-                if (COAL && !__shfl_sync(FULL_MASK, first, q))
-                    continue;
-                if ((unsigned)s >= (unsigned)N) {
-                    if (lane == 0)
-                        report(err_word, MOE_ERRBIT_BAD_INDEX);
-                    continue;
-                }
-                uint8_t *dq = recv_q + (int64_t)s * H;
-                float *ds = recv_scales + (int64_t)s * B;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = c0 + u * 32;
-                    if (c < C) {
-                        st_v2(dq + (int64_t)c * 8, code[u]);
-                        if ((lane & 15) == 0)
-                            ds[c >> 4] = scale[u];
-                    }
-                }
             }
         }
     }
@@ -400,68 +274,6 @@ cudaError_t launch_layout_dispatch(int T, int H, int k, int E, int R, const int3
         return launch_dispatch_bulk<false>(T, H, k, x, slot_of, recv, T * k, true, err_word,
                                            stream);
     return launch_dispatch_bf16(T, H, k, x, slot_of, recv, err_word, stream);
-}
-
-template <int U, bool COAL>
-static cudaError_t launch_fp8_u(int T, int H, int k, const void *x, const int32_t *slot_of,
-                                uint8_t *recv_q, float *recv_scales, int rows,
-                                uint32_t *err_word, cudaStream_t stream)
-{
-    const int C = H / 8;
-    const int groups = (C + 32 * U - 1) / (32 * U);
-    const int64_t items = (int64_t)T * groups;
-    auto kern = dispatch_fp8_kernel<U, COAL>;
-    const int grid = warp_item_grid((const void *)kern, DISPATCH_THREADS, 0, items);
-    return launch_pdl(kern, dim3(grid), dim3(DISPATCH_THREADS), 0, stream,
-                      static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H, groups,
-                      items, rows, err_word);
-}
-
-// Rounds of warp items the busiest warp runs, times the blocks per item: the
-// item time, in units of one block's work, of a launch with U blocks per item.
-template <int U, bool COAL>
-static int64_t fp8_rounds(int T, int H)
-{
-    const int C = H / 8;
-    const int64_t items = (int64_t)T * ((C + 32 * U - 1) / (32 * U));
-    auto kern = dispatch_fp8_kernel<U, COAL>;
-    const int64_t warps = (int64_t)warp_item_grid((const void *)kern, DISPATCH_THREADS, 0,
-                                                  items) * (DISPATCH_THREADS / 32);
-    return (items + warps - 1) / warps * U;
-}
-
-template <bool COAL>
-static cudaError_t launch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
-                              uint8_t *recv_q, float *recv_scales, int rows, uint32_t *err_word,
-                              cudaStream_t stream)
-{
-    if (T == 0)
-        return cudaSuccess;
-    // QUANT_U blocks per warp item keep the most bytes in flight, but a batch
-    // whose items fill the GPU's warps only 1.5 times over (1024 tokens of
-    // 7168 channels: 7168 items on 4864 resident warps) leaves the second
-    // round half empty; items of half the size then finish sooner (3 rounds
-    // of half items, against 2 of whole ones).
-    if (QUANT_U == 4 && fp8_rounds<2, COAL>(T, H) < fp8_rounds<QUANT_U, COAL>(T, H))
-        return launch_fp8_u<2, COAL>(T, H, k, x, slot_of, recv_q, recv_scales, rows, err_word,
-                                     stream);
-    return launch_fp8_u<QUANT_U, COAL>(T, H, k, x, slot_of, recv_q, recv_scales, rows, err_word,
-                                       stream);
-}
-
-cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
-                                uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
-                                cudaStream_t stream)
-{
-    return launch_fp8<false>(T, H, k, x, slot_of, recv_q, recv_scales, T * k, err_word, stream);
-}
-
-cudaError_t launch_dispatch_fp8_coalesced(int T, int H, int k, const void *x,
-                                          const int32_t *crow, uint8_t *recv_q,
-                                          float *recv_scales, int rows, uint32_t *err_word,
-                                          cudaStream_t stream)
-{
-    return launch_fp8<true>(T, H, k, x, crow, recv_q, recv_scales, rows, err_word, stream);
 }
 
 }  // namespace moe

@@ -1,0 +1,212 @@
+// Dispatch with fused FP8-E4M3 block quantisation (sm_103a).
+//
+// UBEP, Table 3: the DeepSeek-R1 / V3.2 deployments run W8A8; the pages give
+// no further recipe.  Reading: per token row, 1 x 128-channel blocks; scale =
+// amax / 448 and inv = 448 / amax, each one correctly rounded fp32 division;
+// code = e4m3(x * inv), one rounded fp32 multiply then a saturating
+// nearest-even conversion.  The token is quantised once and the same codes
+// and scales go to all k slots (or, COAL, once per coalesced row).
+//
+// GPU design: a warp item is one token and 2U blocks of 128 channels; each
+// half-warp owns a block (16 lanes x 8 channels, U 16-byte vectors of x in
+// flight per lane), reduces its amax with xor-shuffles, and stores 8-byte code
+// words and one fp32 scale per block to every destination row.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+constexpr int QUANT_THREADS = 256;
+// 16-lane quantisation blocks per half-warp per item (compile-time tunable;
+// the default is the shipped configuration).  Four keep 64 bytes of x in
+// flight per lane (measured on one GB300, each launch after a flush: 65536
+// tokens, H = 4096, k = 2: 227 us with 2, 204 us with 4; 8192 tokens,
+// H = 7168, k = 8: 104-105 us with either; 6 and 8 were slower at H = 7168).
+#ifndef MOE_QUANT_U
+#define MOE_QUANT_U 4
+#endif
+constexpr int QUANT_U = MOE_QUANT_U;
+
+// FP8: each half-warp owns one 128-channel block (16 lanes x 8 channels).
+// The amax is reduced with xor-shuffles inside the half-warp; scale and
+// reciprocal are each one correctly rounded fp32 division; each channel is one
+// rounded fp32 multiply followed by a saturating nearest-even E4M3 conversion.
+template <int U, bool COAL>
+__global__ void __launch_bounds__(QUANT_THREADS)
+    dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
+                        uint8_t *__restrict__ recv_q, float *__restrict__ recv_scales, int k,
+                        int H, int groups, int64_t items, int N, uint32_t *err_word)
+{
+    wait_prior_grid();
+    allow_next_grid();
+    const int lane = threadIdx.x & 31;
+    const int C = H >> 3;    // 16-byte vectors per row
+    const int B = H >> 7;    // 128-channel blocks per row
+    const int64_t nwarps = (int64_t)gridDim.x * (QUANT_THREADS / 32);
+    for (int64_t it = (int64_t)blockIdx.x * (QUANT_THREADS / 32) + (threadIdx.x >> 5);
+         it < items; it += nwarps) {
+        const int64_t t = it / groups;
+        const int c0 = (int)(it - t * groups) * (32 * U) + lane;
+        const uint4 *src = x + t * C;
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            v[u] = c0 + u * 32 < C ? ld_stream_v4(src + c0 + u * 32) : make_uint4(0, 0, 0, 0);
+
+        uint2 code[U];
+        float scale[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            float f[8];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                f[2 * p] = bf16lo(w[p]);
+                f[2 * p + 1] = bf16hi(w[p]);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, o));
+            bool zero = !(amax > 0.0f);
+            float inv = 0.0f, sc = 1.0f;
+            if (!zero) {
+                inv = __fdiv_rn(448.0f, amax);
+                if (isinf(inv))
+                    zero = true;
+                else
+                    sc = __fdiv_rn(amax, 448.0f);
+            }
+            uint32_t packed[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int i = 4 * h + 2 * p;
+                    uint32_t pair;
+                    if (zero) {
+                        const uint32_t src_w = w[2 * h + p];
+                        pair = ((src_w >> 15) & 1u) << 7 | ((src_w >> 31) & 1u) << 15;
+                    } else {
+                        float2 g;
+                        g.x = __fmul_rn(f[i], inv);
+                        g.y = __fmul_rn(f[i + 1], inv);
+                        pair = __nv_cvt_float2_to_fp8x2(g, __NV_SATFINITE, __NV_E4M3);
+                    }
+                    word |= (pair & 0xffffu) << (16 * p);
+                }
+                packed[h] = word;
+            }
+            code[u] = make_uint2(packed[0], packed[1]);
+            scale[u] = sc;
+        }
+
+        const int32_t *so = slot_of + t * k;
+        for (int jb = 0; jb < k; jb += 32) {
+            const int32_t mine = jb + lane < k ? ld_nc_s32(so + jb + lane) : 0;
+            const int jn = min(32, k - jb);
+            // COAL (k <= 32): a slot whose coalesced row a lower slot of the
+            // token names stores nothing; that row is written once
+            bool first = true;
+            if (COAL) {
+                const unsigned kmask = jn >= 32 ? FULL_MASK : (1u << jn) - 1u;
+                first = (__match_any_sync(FULL_MASK, mine) & kmask & lanemask_lt()) == 0;
+            }
+            for (int q = 0; q < jn; ++q) {
+                const int32_t s = __shfl_sync(FULL_MASK, mine, q);
+                if (COAL && !__shfl_sync(FULL_MASK, first, q))
+                    continue;
+                if ((unsigned)s >= (unsigned)N) {
+                    if (lane == 0)
+                        report(err_word, MOE_ERRBIT_BAD_INDEX);
+                    continue;
+                }
+                uint8_t *dq = recv_q + (int64_t)s * H;
+                float *ds = recv_scales + (int64_t)s * B;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + u * 32;
+                    if (c < C) {
+                        st_v2(dq + (int64_t)c * 8, code[u]);
+                        if ((lane & 15) == 0)
+                            ds[c >> 4] = scale[u];
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int U, bool COAL>
+static cudaError_t launch_fp8_u(int T, int H, int k, const void *x, const int32_t *slot_of,
+                                uint8_t *recv_q, float *recv_scales, int rows,
+                                uint32_t *err_word, cudaStream_t stream)
+{
+    const int C = H / 8;
+    const int groups = (C + 32 * U - 1) / (32 * U);
+    const int64_t items = (int64_t)T * groups;
+    auto kern = dispatch_fp8_kernel<U, COAL>;
+    const int grid = warp_item_grid((const void *)kern, QUANT_THREADS, 0, items);
+    return launch_pdl(kern, dim3(grid), dim3(QUANT_THREADS), 0, stream,
+                      static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H, groups,
+                      items, rows, err_word);
+}
+
+// Rounds of warp items the busiest warp runs, times the blocks per item: the
+// item time, in units of one block's work, of a launch with U blocks per item.
+template <int U, bool COAL>
+static int64_t fp8_rounds(int T, int H)
+{
+    const int C = H / 8;
+    const int64_t items = (int64_t)T * ((C + 32 * U - 1) / (32 * U));
+    auto kern = dispatch_fp8_kernel<U, COAL>;
+    const int64_t warps = (int64_t)warp_item_grid((const void *)kern, QUANT_THREADS, 0,
+                                                  items) * (QUANT_THREADS / 32);
+    return (items + warps - 1) / warps * U;
+}
+
+template <bool COAL>
+static cudaError_t launch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
+                              uint8_t *recv_q, float *recv_scales, int rows, uint32_t *err_word,
+                              cudaStream_t stream)
+{
+    if (T == 0)
+        return cudaSuccess;
+    // QUANT_U blocks per warp item keep the most bytes in flight, but a batch
+    // whose items fill the GPU's warps only 1.5 times over (1024 tokens of
+    // 7168 channels: 7168 items on 4864 resident warps) leaves the second
+    // round half empty; items of half the size then finish sooner (3 rounds
+    // of half items, against 2 of whole ones).  Only while the whole items
+    // take a few rounds: over many rounds the half items' fixed costs weigh
+    // more than the last round's idle warps (measured: 65536 tokens of 4096
+    // channels, 203 us with whole items, 227 us with half items).
+    const int64_t whole = fp8_rounds<QUANT_U, COAL>(T, H);
+    if (QUANT_U == 4 && whole <= 3 * QUANT_U && fp8_rounds<2, COAL>(T, H) < whole)
+        return launch_fp8_u<2, COAL>(T, H, k, x, slot_of, recv_q, recv_scales, rows, err_word,
+                                     stream);
+    return launch_fp8_u<QUANT_U, COAL>(T, H, k, x, slot_of, recv_q, recv_scales, rows, err_word,
+                                       stream);
+}
+
+cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
+                                uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
+                                cudaStream_t stream)
+{
+    return launch_fp8<false>(T, H, k, x, slot_of, recv_q, recv_scales, T * k, err_word, stream);
+}
+
+cudaError_t launch_dispatch_fp8_coalesced(int T, int H, int k, const void *x,
+                                          const int32_t *crow, uint8_t *recv_q,
+                                          float *recv_scales, int rows, uint32_t *err_word,
+                                          cudaStream_t stream)
+{
+    return launch_fp8<true>(T, H, k, x, crow, recv_q, recv_scales, rows, err_word, stream);
+}
+
+}  // namespace moe

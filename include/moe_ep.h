@@ -9,7 +9,9 @@
  *
  * Conventions for every entry point:
  *   - All array pointers are DEVICE pointers owned by the caller.  The library
- *     never allocates, frees or keeps a pointer past the call.
+ *     never allocates, frees or keeps a pointer past the call.  The output
+ *     arrays of a call may not overlap one another or its inputs (the kernels
+ *     are compiled on that promise).
  *   - Every call is asynchronous and ordered on `stream`; none copies data back
  *     to the host.  MOE_OK means the work was enqueued.
  *   - Arguments are checked before anything is launched; a bad argument returns
