@@ -514,7 +514,8 @@ __all__ = [
     "moe_combine_backward", "moe_dispatch_backward",
     "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_dispatch_quant_coalesced",
     "moe_combine_coalesced",
-    "moe_dispatch_combine_flagged", "LIB_PATH", "SIGNATURES",
+    "moe_dispatch_combine_flagged", "moe_ep_reorder", "moe_layout_last_form", "LIB_PATH",
+    "SIGNATURES",
 ]
 
 
