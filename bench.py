@@ -467,7 +467,7 @@ class StepBench:
     and is not charged for the dispatch's write-backs).  Both flushes sit
     outside the events."""
 
-    def __init__(self, name, dev, seed, variant, m, keep_host=False):
+    def __init__(self, name, dev, seed, variant, m, stream=None):
         import torch
         import ctypes
         from workloads.gen import make_workload, CONFIGS, device_inputs
@@ -513,7 +513,7 @@ class StepBench:
         # on GB300 (combine then pays ~1.6 us of their write-back); one read of
         # 4xL2 evicts them all.
         self.flush_r = torch.zeros(max(4 * l2, 512 << 20), dtype=torch.uint8, device=dev)
-        self.stream = torch.cuda.current_stream(dev)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
 
         # The step calls the C ABI directly with pre-marshalled arguments, so
         # host time between launches stays far below the GPU time of a step.

@@ -299,7 +299,9 @@ def test_combine_f32_matches_oracle(name):
 
 
 COMBINE_FUZZ = [(41, 1, 8, 1, 1, 1), (42, 50, 264, 3, 5, 5), (43, 333, 2048, 8, 64, 8),
-                (44, 77, 7176, 6, 12, 3), (45, 9, 64, 40, 7, 7), (46, 2000, 4096, 2, 8, 8)]
+                (44, 77, 7176, 6, 12, 3), (45, 9, 64, 40, 7, 7), (46, 2000, 4096, 2, 8, 8),
+                # k > 32 (the register fallback): several row batches, ragged H
+                (47, 300, 7168, 40, 256, 32), (48, 50, 1000, 64, 64, 8), (49, 33, 2056, 33, 33, 11)]
 
 
 @pytest.mark.parametrize("case", COMBINE_FUZZ, ids=[f"s{c[0]}_T{c[1]}_H{c[2]}_k{c[3]}" for c in COMBINE_FUZZ])
