@@ -755,10 +755,10 @@ def run_gpu(args):
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
-    if world > 1 and not dist.is_initialized():
+    if (world > 1 or args.ep_nccl) and not dist.is_initialized():
         import datetime
         dist.init_process_group("nccl", timeout=datetime.timedelta(seconds=180))
-    if world > 1 or args.ep_virtual > 1:
+    if world > 1 or args.ep_nccl or args.ep_virtual > 1:
         return run_gpu_ep(args, rank, world, local)
     dev = torch.device("cuda", local)
 
@@ -897,7 +897,7 @@ def run_gpu_ep(args, rank, world, local):
 
     dev = torch.device("cuda", local)
     name = args.config
-    virtual = world == 1
+    virtual = world == 1 and not args.ep_nccl
     W = args.ep_virtual if virtual else world
     err = m.new_error_word(dev)
     ops = ep.LibraryOps(err)
@@ -1363,6 +1363,9 @@ def main(argv=None):
                         "dispatch_coalesced, combine_coalesced, ep_reorder")
     p.add_argument("--shape", default=None, help="with --profile-op: T,H,k,E,R of a uniform "
                                                  "random routing instead of --config")
+    p.add_argument("--ep-nccl", action="store_true",
+                   help="run the expert-parallel step through an NCCL process group even with "
+                        "one rank (under torchrun), to exercise the exchange on one GPU")
     p.add_argument("--ep-virtual", type=int, default=1,
                    help="on one GPU: time expert parallelism over W virtual ranks (the "
                         "exchange done by device copies) instead of the single-GPU step")
