@@ -557,6 +557,14 @@ class StepBench:
                            P(lay.expert_offsets), P(lay.rank_offsets), P(lay.slot_of),
                            P(lay.src_of), P(self.recv) if self.fused_front else None, P(self.ws),
                            self.ws.numel(), P(err), cs)
+        # FP8: layout then the FP8 dispatch as one call, the dispatch's first
+        # loads and quantisation of x overlapping the layout
+        self.fused_front_quant = self.fp8 and not self.coal
+        self.front_quant_args = (T, H, k, E, R, P(self.idx), P(x), P(lay.expert_counts),
+                                 P(lay.expert_offsets), P(lay.rank_offsets), P(lay.slot_of),
+                                 P(lay.src_of), P(self.recv_q) if self.fp8 else None,
+                                 P(self.recv_s) if self.fp8 else None, P(self.ws),
+                                 self.ws.numel(), P(err), cs)
         self.d_name = (("dispatch_fp8_coalesced" if self.fp8 else "dispatch_coalesced")
                        if self.coal else ("dispatch_fp8" if self.fp8 else "dispatch_bf16"))
         self.c_name = "combine_coalesced" if self.coal else "combine"
@@ -578,6 +586,8 @@ class StepBench:
     def front(self):
         if self.fused_front:
             self._call(self.L.moe_layout_dispatch, self.front_args)
+        elif self.fused_front_quant:
+            self._call(self.L.moe_layout_dispatch_quant, self.front_quant_args)
         else:
             self.layout_only()
             self.dispatch_only()
@@ -709,6 +719,7 @@ def per_config_entry(b: StepBench, r: dict, peak: float) -> dict:
         "dispatch": dict(_frac(b.bytes_of("front"), front, peak),
                          what="layout + dispatch in the timed steps (A1-A4 or A1-A3 + A5)",
                          call="moe_layout_dispatch" if b.fused_front else
+                              "moe_layout_dispatch_quant" if b.fused_front_quant else
                               f"moe_layout + {b.disp[0].__name__}"),
         "dispatch_kernel": dict(_frac(b.bytes_of(b.d_name), disp, peak),
                                 what="the dispatch kernel alone, breakdown pass"),
@@ -1076,8 +1087,8 @@ def e2e_leg(b: StepBench, args, world):
                 m.moe_combine_coalesced(y, lay.slot_of, wb[j], co, b.rows, partial=b.partial,
                                         out=ob[j], err_word=err, stream=stream)
             else:
-                m.moe_layout(ib[j], E, R, workspace=ws, err_word=err, out=lay, stream=stream)
-                m.moe_dispatch_quant(xb[j], lay.slot_of, err_word=err, stream=stream, **rq)
+                m.moe_layout_dispatch_quant(xb[j], ib[j], E, R, workspace=ws, out=lay,
+                                            err_word=err, stream=stream, **rq)
                 m.moe_combine(y, lay.slot_of, wb[j], out=ob[j], err_word=err, stream=stream)
             comp_done[i].record(stream)
             with torch.cuda.stream(d2h_s):
@@ -1277,6 +1288,11 @@ def run_profile_op(args):
     elif op == "dispatch":
         recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
         fn = lambda: m.moe_dispatch(x, lay.slot_of, recv=recv, **kw)  # noqa: E731
+    elif op == "layout_dispatch_quant":
+        rq = torch.empty((N, H), dtype=torch.uint8, device=dev)
+        rs = torch.empty((N, H // 128), dtype=torch.float32, device=dev)
+        fn = lambda: m.moe_layout_dispatch_quant(x, idx, E, R, workspace=ws, out=lay,  # noqa: E731
+                                                 recv_q=rq, recv_scales=rs, **kw)
     elif op == "dispatch_fp8":
         rq = torch.empty((N, H), dtype=torch.uint8, device=dev)
         rs = torch.empty((N, H // 128), dtype=torch.float32, device=dev)
@@ -1358,7 +1374,8 @@ def main(argv=None):
     p.add_argument("--no-per-config", action="store_true")
     p.add_argument("--profile-op", default=None,
                    help="time one entry point alone on --config (or --shape), for ncu "
-                        "captures: layout, layout_dispatch, dispatch, dispatch_fp8, combine, "
+                        "captures: layout, layout_dispatch, layout_dispatch_quant, dispatch, "
+                        "dispatch_fp8, combine, "
                         "combine_backward, dispatch_backward, layout_coalesced, "
                         "dispatch_coalesced, combine_coalesced, ep_reorder")
     p.add_argument("--shape", default=None, help="with --profile-op: T,H,k,E,R of a uniform "

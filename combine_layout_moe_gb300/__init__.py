@@ -40,6 +40,8 @@ SIGNATURES = {
     "moe_layout_dispatch": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P,
                              _P], ctypes.c_int),
     "moe_dispatch_quant": ([_I, _I, _I, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
+    "moe_layout_dispatch_quant": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _SZ, _U32P, _P], ctypes.c_int),
     "moe_combine": ([_I, _I, _I, _P, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_read_error": ([_U32P, _I, _P, ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     "moe_layout_noalloc": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
@@ -325,6 +327,46 @@ def moe_layout_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, E: int, R: int,
     return out, recv
 
 
+def moe_layout_dispatch_quant(x: torch.Tensor, topk_idx: torch.Tensor, E: int, R: int, *,
+                              workspace: Optional[torch.Tensor] = None,
+                              out: Optional[Layout] = None,
+                              recv_q: Optional[torch.Tensor] = None,
+                              recv_scales: Optional[torch.Tensor] = None,
+                              err_word: Optional[torch.Tensor] = None,
+                              stream: Optional[torch.cuda.Stream] = None):
+    """moe_layout then moe_dispatch_quant, the FP8 dispatch's first loads and
+    quantisation of x overlapping the layout.  Returns (Layout, recv_q uint8
+    [T*k, H], recv_scales fp32 [T*k, H/128])."""
+    if topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be [T, k]")
+    T, k = topk_idx.shape
+    H = x.shape[1]
+    _want(topk_idx, "topk_idx", torch.int32)
+    _want(x, "x", torch.bfloat16, (T, H))
+    dev = topk_idx.device
+    if out is None:
+        out = Layout(torch.empty(E, dtype=torch.int32, device=dev),
+                     torch.empty(E + 1, dtype=torch.int32, device=dev),
+                     torch.empty(R + 1, dtype=torch.int32, device=dev),
+                     torch.empty((T, k), dtype=torch.int32, device=dev),
+                     torch.empty(T * k, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = new_workspace(moe_layout_workspace_bytes(T, k, E), dev)
+    if recv_q is None:
+        recv_q = torch.empty((T * k, H), dtype=torch.uint8, device=dev)
+    if recv_scales is None:
+        recv_scales = torch.empty((T * k, H // 128), dtype=torch.float32, device=dev)
+    _check(_lib.moe_layout_dispatch_quant(T, H, k, E, R, _ptr(topk_idx), _ptr(x),
+                                          _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                          _ptr(out.rank_offsets), _ptr(out.slot_of),
+                                          _ptr(out.src_of), _ptr(recv_q), _ptr(recv_scales),
+                                          _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _ptr(err_word), _stream(stream)),
+           "moe_layout_dispatch_quant")
+    return out, recv_q, recv_scales
+
+
 def moe_dispatch(x: torch.Tensor, slot_of: torch.Tensor, *, recv: Optional[torch.Tensor] = None,
                  err_word: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
@@ -509,7 +551,7 @@ def moe_read_error(err_word: torch.Tensor, clear: bool = True,
 __all__ = [
     "Layout", "MoeError", "moe_abi_version", "moe_status_string", "new_error_word", "new_workspace",
     "moe_layout_workspace_bytes", "moe_layout", "moe_layout_noalloc", "moe_dispatch", "moe_dispatch_quant",
-    "moe_layout_dispatch",
+    "moe_layout_dispatch", "moe_layout_dispatch_quant",
     "moe_combine", "moe_read_error", "moe_sync_words", "SyncState",
     "moe_combine_backward", "moe_dispatch_backward",
     "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_dispatch_quant_coalesced",

@@ -233,6 +233,35 @@ moe_status moe_layout_dispatch(int T, int H, int k, int E, int R, const int32_t 
                                                  recv, workspace, err_word, stream));
 }
 
+moe_status moe_layout_dispatch_quant(int T, int H, int k, int E, int R, const int32_t *topk_idx,
+                                     const void *x, int32_t *expert_counts,
+                                     int32_t *expert_offsets, int32_t *rank_offsets,
+                                     int32_t *slot_of, int32_t *src_of, uint8_t *recv_q,
+                                     float *recv_scales, void *workspace, size_t workspace_bytes,
+                                     uint32_t *err_word, cudaStream_t stream)
+{
+    if (!pairs_ok(T, k) || E < 1 || R < 1 || E % R != 0 || H < 128 || H % 128 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (E > MOE_MAX_EXPERTS)
+        return MOE_ERR_UNSUPPORTED;
+    if (!expert_counts || !expert_offsets || !rank_offsets)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !x || !slot_of || !src_of || !recv_q || !recv_scales ||
+                  !workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 4) || !aligned(expert_counts, 4) || !aligned(expert_offsets, 4) ||
+        !aligned(rank_offsets, 4) || !aligned(slot_of, 4) || !aligned(src_of, 4) ||
+        !aligned(workspace, 16) || !aligned(x, 16) || !aligned(recv_q, 16) ||
+        !aligned(recv_scales, 16) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && workspace_bytes < moe::layout_workspace_bytes((int64_t)T * k, E))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_layout_dispatch_quant(T, H, k, E, R, topk_idx, x, expert_counts,
+                                                       expert_offsets, rank_offsets, slot_of,
+                                                       src_of, recv_q, recv_scales, workspace,
+                                                       err_word, stream));
+}
+
 moe_status moe_dispatch_quant(int T, int H, int k, const void *x, const int32_t *slot_of,
                               uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
                               cudaStream_t stream)

@@ -37,10 +37,19 @@ template <int U, bool COAL>
 __global__ void __launch_bounds__(QUANT_THREADS)
     dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
                         uint8_t *__restrict__ recv_q, float *__restrict__ recv_scales, int k,
-                        int H, int groups, int64_t items, int N, uint32_t *err_word)
+                        int H, int groups, int64_t items, int N, int prefetch_x,
+                        uint32_t *err_word)
 {
-    wait_prior_grid();
-    allow_next_grid();
+    // prefetch_x: the first item's x is loaded and quantised before waiting
+    // for the previous grid, and only the slot map and the stores wait.  Only
+    // for a launch whose previous grid is this library's layout kernel: that
+    // kernel lets dependents launch only after its own wait, so x and the
+    // receive buffers are final; the slot map is not.
+    bool waited = !prefetch_x;
+    if (waited) {
+        wait_prior_grid();
+        allow_next_grid();
+    }
     const int lane = threadIdx.x & 31;
     const int C = H >> 3;    // 16-byte vectors per row
     const int B = H >> 7;    // 128-channel blocks per row
@@ -107,6 +116,11 @@ __global__ void __launch_bounds__(QUANT_THREADS)
             scale[u] = sc;
         }
 
+        if (!waited) {
+            wait_prior_grid();
+            allow_next_grid();
+            waited = true;
+        }
         const int32_t *so = slot_of + t * k;
         for (int jb = 0; jb < k; jb += 32) {
             const int32_t mine = jb + lane < k ? ld_nc_s32(so + jb + lane) : 0;
@@ -141,11 +155,15 @@ __global__ void __launch_bounds__(QUANT_THREADS)
             }
         }
     }
+    if (!waited) {  // a warp with no item still lets the next grid launch
+        wait_prior_grid();
+        allow_next_grid();
+    }
 }
 
 template <int U, bool COAL>
 static cudaError_t launch_fp8_u(int T, int H, int k, const void *x, const int32_t *slot_of,
-                                uint8_t *recv_q, float *recv_scales, int rows,
+                                uint8_t *recv_q, float *recv_scales, int rows, bool prefetch_x,
                                 uint32_t *err_word, cudaStream_t stream)
 {
     const int C = H / 8;
@@ -155,7 +173,7 @@ static cudaError_t launch_fp8_u(int T, int H, int k, const void *x, const int32_
     const int grid = warp_item_grid((const void *)kern, QUANT_THREADS, 0, items);
     return launch_pdl(kern, dim3(grid), dim3(QUANT_THREADS), 0, stream,
                       static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H, groups,
-                      items, rows, err_word);
+                      items, rows, prefetch_x ? 1 : 0, err_word);
 }
 
 // Rounds of warp items the busiest warp runs, times the blocks per item: the
@@ -174,7 +192,7 @@ static int64_t fp8_rounds(int T, int H)
 template <bool COAL>
 static cudaError_t launch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
                               uint8_t *recv_q, float *recv_scales, int rows, uint32_t *err_word,
-                              cudaStream_t stream)
+                              cudaStream_t stream, bool prefetch_x = false)
 {
     if (T == 0)
         return cudaSuccess;
@@ -188,10 +206,10 @@ static cudaError_t launch_fp8(int T, int H, int k, const void *x, const int32_t 
     // channels, 203 us with whole items, 227 us with half items).
     const int64_t whole = fp8_rounds<QUANT_U, COAL>(T, H);
     if (QUANT_U == 4 && whole <= 3 * QUANT_U && fp8_rounds<2, COAL>(T, H) < whole)
-        return launch_fp8_u<2, COAL>(T, H, k, x, slot_of, recv_q, recv_scales, rows, err_word,
-                                     stream);
-    return launch_fp8_u<QUANT_U, COAL>(T, H, k, x, slot_of, recv_q, recv_scales, rows, err_word,
-                                       stream);
+        return launch_fp8_u<2, COAL>(T, H, k, x, slot_of, recv_q, recv_scales, rows, prefetch_x,
+                                     err_word, stream);
+    return launch_fp8_u<QUANT_U, COAL>(T, H, k, x, slot_of, recv_q, recv_scales, rows,
+                                       prefetch_x, err_word, stream);
 }
 
 cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
@@ -207,6 +225,23 @@ cudaError_t launch_dispatch_fp8_coalesced(int T, int H, int k, const void *x,
                                           cudaStream_t stream)
 {
     return launch_fp8<true>(T, H, k, x, crow, recv_q, recv_scales, rows, err_word, stream);
+}
+
+cudaError_t launch_layout_dispatch_quant(int T, int H, int k, int E, int R,
+                                         const int32_t *topk_idx, const void *x,
+                                         int32_t *expert_counts, int32_t *expert_offsets,
+                                         int32_t *rank_offsets, int32_t *slot_of,
+                                         int32_t *src_of, uint8_t *recv_q, float *recv_scales,
+                                         void *workspace, uint32_t *err_word,
+                                         cudaStream_t stream)
+{
+    cudaError_t e = launch_layout(T, k, E, R, topk_idx, expert_counts, expert_offsets,
+                                  rank_offsets, slot_of, src_of, workspace, err_word, stream);
+    if (e != cudaSuccess || T == 0)
+        return e;
+    // the layout kernel is the previous grid: x may be read early
+    return launch_fp8<false>(T, H, k, x, slot_of, recv_q, recv_scales, T * k, err_word, stream,
+                             true);
 }
 
 }  // namespace moe

@@ -52,6 +52,16 @@ cudaError_t launch_layout_dispatch_fused(int T, int H, int k, int E, int R,
                                          int32_t *src_of, void *recv, uint32_t *err_word,
                                          cudaStream_t stream);
 
+// moe_layout followed by moe_dispatch_quant, whose first items' loads and
+// quantisation of x overlap the layout.
+cudaError_t launch_layout_dispatch_quant(int T, int H, int k, int E, int R,
+                                         const int32_t *topk_idx, const void *x,
+                                         int32_t *expert_counts, int32_t *expert_offsets,
+                                         int32_t *rank_offsets, int32_t *slot_of,
+                                         int32_t *src_of, uint8_t *recv_q, float *recv_scales,
+                                         void *workspace, uint32_t *err_word,
+                                         cudaStream_t stream);
+
 cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
                                 uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
                                 cudaStream_t stream);

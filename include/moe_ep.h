@@ -184,6 +184,25 @@ MOE_API moe_status moe_dispatch_quant(int T, int H, int k, const void *x, const 
                               cudaStream_t stream);
 
 /*
+ * moe_layout_dispatch_quant -- moe_layout followed by moe_dispatch_quant, with
+ * the dispatch's first loads and quantisation of x overlapping the layout.
+ *
+ * UBEP, section 3.2 (token sending overlaps the count and scan) and Table 3
+ * (W8A8).  Same arguments, outputs, rules and errors as moe_layout and
+ * moe_dispatch_quant called in turn on `stream`.  The FP8 dispatch kernel
+ * launches while the layout kernel runs, loads and quantises its first token
+ * blocks, and waits for the layout only before reading the slot map; x must
+ * be complete before this call, as for moe_dispatch_quant.
+ */
+MOE_API moe_status moe_layout_dispatch_quant(int T, int H, int k, int E, int R,
+                                     const int32_t *topk_idx, const void *x,
+                                     int32_t *expert_counts, int32_t *expert_offsets,
+                                     int32_t *rank_offsets, int32_t *slot_of, int32_t *src_of,
+                                     uint8_t *recv_q, float *recv_scales, void *workspace,
+                                     size_t workspace_bytes, uint32_t *err_word,
+                                     cudaStream_t stream);
+
+/*
  * moe_combine -- gather expert outputs back to token order, router-weighted.
  *
  * HyperParallel-MoE, section 2.2 (expert outputs are weighted by the routing

@@ -425,3 +425,36 @@ def test_layout_dispatch_single_kernel_bad_id():
     want = np.full(idx.size, -1, np.int64)
     want[order] = np.arange(good.sum())
     assert np.array_equal(so.ravel(), want)
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3_decode", "dsv3_prefill", "glm45_air", "mixtral"])
+def test_layout_dispatch_quant_matches_oracle(name):
+    """The combined FP8 call, whose dispatch loads and quantises x while the
+    layout still runs: the layout, codes and scales of the two calls in turn."""
+    m = cl()
+    w = workload(name)
+    err = m.new_error_word()
+    lay, q, sc = m.moe_layout_dispatch_quant(bf16_dev(w.x), i32_dev(w.topk_idx), w.E, w.R,
+                                             err_word=err)
+    assert m.moe_read_error(err) == 0
+    o = oracle.layout(w.topk_idx, w.E, w.R)
+    for a, b in zip(lay, o):
+        assert np.array_equal(a.cpu().numpy(), b)
+    rq, rs = oracle.dispatch_quant(w.x, o[3])
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(sc.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("case", [(91, 1, 128, 1, 1, 1), (92, 3000, 1024, 3, 12, 4),
+                                  (93, 20000, 256, 8, 64, 8), (94, 0, 128, 2, 4, 2)])
+def test_layout_dispatch_quant_fuzz(case):
+    m = cl()
+    seed, T, H, k, E, R = case
+    w = random_case(seed, T, H, k, E, R)
+    lay, q, sc = m.moe_layout_dispatch_quant(bf16_dev(w.x), i32_dev(w.topk_idx), E, R)
+    torch.cuda.synchronize()
+    o = oracle.layout(w.topk_idx, E, R)
+    assert np.array_equal(lay.slot_of.cpu().numpy(), o[3])
+    rq, rs = oracle.dispatch_quant(w.x, o[3])
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(sc.cpu().numpy(), rs)
