@@ -808,9 +808,6 @@ def run_gpu(args):
     tr = None if coal else recorded_traffic(kern_name, name)
     traffic = tr.get("dram_bytes_per_launch") if tr is not None else None
 
-    write_ceiling = None
-    if dom.startswith("dispatch") and b.recv is not None:
-        write_ceiling = measure_write_ceiling(b, dom_ms, args.steps)
     launches = b.launches_per_step() * args.steps
     e2e = e2e_leg(b, args, world)
     headline = per_config_entry(b, r, peak)
@@ -865,8 +862,7 @@ def run_gpu(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "traffic_source": tr.get("capture") if tr is not None else None,
                      "algorithmic_bytes": dom_bytes, "duration_ms": dom_ms,
-                     "duration_source": source,
-                     "write_ceiling": write_ceiling},
+                     "duration_source": source},
         "segments_ms": {"layout+" + b_dname(fp8, coal): statistics.mean(t_front),
                         "combine": avg_c},
         "kernels_ms": {"layout": statistics.mean(r["t_layout"]), b_dname(fp8, coal): avg_d,
@@ -987,35 +983,6 @@ def run_gpu_ep(args, rank, world, local):
         "clocks": nv.summary(),
     }
     print(json.dumps(line), flush=True)
-
-
-def measure_write_ceiling(b, dispatch_ms, reps):
-    """The dispatch writes k rows per token read, and on GB300 a stream of
-    writes alone runs well below the copy rate that `peak` is: time torch's
-    fill of the same receive buffer (the dispatch's written bytes, nothing
-    read) in the same regime (after a 2xL2 write, CUDA events on the stream)
-    and compare the dispatch with it."""
-    import torch
-    ev = []
-    for i in range(3 + max(3, min(reps, 50))):
-        b.dirty_flush()
-        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(b.stream)
-        b.recv.fill_(0.0)
-        c.record(b.stream)
-        if i >= 3:
-            ev.append((a, c))
-    torch.cuda.synchronize()
-    fill_ms = statistics.median(x.elapsed_time(y) for x, y in ev)
-    wbytes = b.recv.numel() * b.recv.element_size()
-    return {"fill_ms": fill_ms, "fill_bytes": wbytes,
-            "fill_gbs": wbytes / (fill_ms / 1000.0) / 1e9,
-            "dispatch_write_gbs": wbytes / (dispatch_ms / 1000.0) / 1e9,
-            "dispatch_vs_fill": fill_ms / dispatch_ms,
-            "how": "torch fill_ of the receive buffer (write-only, same bytes the dispatch "
-                   "writes) after the same 2xL2 write; dispatch_vs_fill > 1 means the "
-                   "dispatch writes its rows (and reads x) faster than a plain fill writes "
-                   "them"}
 
 
 def b_dname(fp8, coal):
