@@ -1332,7 +1332,7 @@ def main(argv=None):
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-budget", type=float, default=12.0)
-    p.add_argument("--ref-tokens", type=int, default=64,
+    p.add_argument("--ref-tokens", type=int, default=2048,
                    help="tokens per oracle step in --impl reference")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--per-config", default=PER_CONFIG,
