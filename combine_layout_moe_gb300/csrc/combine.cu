@@ -551,9 +551,22 @@ constexpr int CB_WARPS = 8;
 #ifndef MOE_CB_MINB
 #define MOE_CB_MINB 3
 #endif
+// For 9 <= k <= 16 an instance sized to 16 slots at three resident blocks
+// (80 registers and 220 bytes of spills; the k <= 32 instance needs 151
+// registers and runs one block): measured
+// on one GB300, each launch after a flush, 4096 tokens, H = 4096: k = 16 379
+// -> 226 us, k = 12 346 -> 184 us; 2048 tokens, H = 7168, k = 10: 291 ->
+// 158 us (one block of the 16-slot instance: 234, 203, 166 us).
+#ifndef MOE_CB16_MINB
+#define MOE_CB16_MINB 3
+#endif
+#ifndef MOE_CB_K16
+#define MOE_CB_K16 1
+#endif
 
 template <int KMAX>
-__global__ void __launch_bounds__(32 * CB_WARPS, KMAX <= 8 ? MOE_CB_MINB : 1)
+__global__ void __launch_bounds__(32 * CB_WARPS,
+                                  KMAX <= 8 ? MOE_CB_MINB : KMAX <= 16 ? MOE_CB16_MINB : 1)
     combine_backward_kernel(const uint4 *__restrict__ dout, const uint4 *__restrict__ y,
                             const int32_t *__restrict__ slot_of, const float *__restrict__ topk_w,
                             uint4 *__restrict__ dy, float *__restrict__ dw, int T, int k, int C,
@@ -1154,6 +1167,9 @@ cudaError_t launch_combine_backward(int T, int H, int k, const void *dout, const
         return launch_combine_backward_t<8>(T, H, k, dout, y, slot_of, topk_w, dy, dw, err_word,
                                             stream);
     }
+    if (MOE_CB_K16 && k <= 16)
+        return launch_combine_backward_t<16>(T, H, k, dout, y, slot_of, topk_w, dy, dw,
+                                             err_word, stream);
     return launch_combine_backward_t<32>(T, H, k, dout, y, slot_of, topk_w, dy, dw, err_word,
                                          stream);
 }

@@ -68,7 +68,9 @@ FUZZ = [(71, 1, 8, 1, 1, 1), (72, 33, 264, 3, 5, 5), (73, 100, 7176, 8, 16, 4),
         (79, 7, 4096, 6, 12, 3), (80, 3001, 136, 7, 7, 7), (81, 1, 16384, 8, 8, 2),
         # H = 262144: the pipeline's ring and stages exceed shared memory, so
         # the CTA-per-token kernel takes k = 8
-        (82, 2, 262144, 8, 8, 2)]
+        (82, 2, 262144, 8, 8, 2),
+        # 9 <= k <= 16: the CTA-per-token kernel's 16-slot instance
+        (83, 300, 2056, 9, 18, 6), (84, 64, 4096, 12, 48, 8)]
 
 
 @pytest.mark.parametrize("case", FUZZ, ids=[f"T{c[1]}_H{c[2]}_k{c[3]}" for c in FUZZ])
