@@ -59,6 +59,7 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "mixtral"
 # the workloads the target names (configs 1-4), measured after the headline
 PER_CONFIG = "dsv3_decode,dsv3_prefill,glm45_air,mixtral"
+PER_CONFIG_MIN_STEPS = 500
 
 
 # ------------------------------------------------------------------ bytes
@@ -830,7 +831,11 @@ def run_gpu(args):
             if not other or other == name:
                 continue
             bo = StepBench(other, dev, args.seed + rank, "plain", m)
-            ro = bo.timed(args.steps, args.warmup, clocks_uuid=uuid)
+            # the other workloads are context for the headline: timed over at
+            # least PER_CONFIG_MIN_STEPS steps, so a short headline run (the
+            # decode step is ~55 us of GPU time) still gives stable averages
+            ro = bo.timed(max(args.steps, PER_CONFIG_MIN_STEPS), max(args.warmup, 20),
+                          clocks_uuid=uuid)
             per_config[other] = per_config_entry(bo, ro, peak)
             per_config[other]["clocks"] = ro["clocks"]
             if want_cpu:
