@@ -47,6 +47,7 @@ SIGNATURES = {
     "moe_layout_noalloc": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_sync_words": ([_I, _I, _I, _I, _I], ctypes.c_size_t),
     "moe_layout_last_form": ([], ctypes.c_int),
+    "moe_e4m3_encode_bits": ([ctypes.c_uint32, ctypes.c_uint32, _P, _P], ctypes.c_int),
     "moe_ep_reorder": ([_I, _I, _I, _P, _I, _P, _P, _I, _P, _U32P, _P], ctypes.c_int),
     "moe_combine_backward": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_dispatch_backward": ([_I, _I, _I, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
@@ -116,6 +117,17 @@ def moe_abi_version() -> int:
 
 def moe_status_string(status: int) -> str:
     return _lib.moe_status_string(status).decode()
+
+
+def moe_e4m3_encode_bits(first: int, count: int, out: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The quantised dispatch's E4M3 encoding of the fp32 values with bit
+    patterns first .. first + count - 1 (uint8 device tensor [count])."""
+    if out is None:
+        out = torch.empty(count, dtype=torch.uint8, device="cuda")
+    _check(_lib.moe_e4m3_encode_bits(first & 0xffffffff, count, _ptr(out), _stream(stream)),
+           "moe_e4m3_encode_bits")
+    return out
 
 
 def moe_layout_last_form() -> int:
@@ -556,7 +568,8 @@ __all__ = [
     "moe_combine_backward", "moe_dispatch_backward",
     "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_dispatch_quant_coalesced",
     "moe_combine_coalesced",
-    "moe_dispatch_combine_flagged", "moe_ep_reorder", "moe_layout_last_form", "LIB_PATH",
+    "moe_dispatch_combine_flagged", "moe_ep_reorder", "moe_layout_last_form",
+    "moe_e4m3_encode_bits", "LIB_PATH",
     "SIGNATURES",
 ]
 

@@ -386,6 +386,14 @@ moe_status moe_ep_reorder(int W, int El, int H, const int32_t *recv_counts, int 
                                             err_word, stream));
 }
 
+moe_status moe_e4m3_encode_bits(uint32_t first, uint32_t count, uint8_t *codes,
+                                cudaStream_t stream)
+{
+    if (count > 0 && !codes)
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_e4m3_bits(first, count, codes, stream));
+}
+
 moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t stream, uint32_t *bits_out)
 {
     if (!err_word || !aligned(err_word, 4))

@@ -19,6 +19,18 @@
 namespace moe {
 
 constexpr int QUANT_THREADS = 256;
+
+// The channel encoding of the quantised dispatch: two fp32 values to two
+// E4M3 codes (low byte first), nearest-even, saturating to +-448.  One
+// routine for the kernel and for moe_e4m3_encode_bits, the diagnostic entry
+// point that lets the tests check it on every fp32 input.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
+{
+    float2 g;
+    g.x = lo;
+    g.y = hi;
+    return __nv_cvt_float2_to_fp8x2(g, __NV_SATFINITE, __NV_E4M3) & 0xffffu;
+}
 // 16-lane quantisation blocks per half-warp per item (compile-time tunable;
 // the default is the shipped configuration).  Four keep 64 bytes of x in
 // flight per lane (measured on one GB300, each launch after a flush: 65536
@@ -103,10 +115,7 @@ __global__ void __launch_bounds__(QUANT_THREADS)
                         const uint32_t src_w = w[2 * h + p];
                         pair = ((src_w >> 15) & 1u) << 7 | ((src_w >> 31) & 1u) << 15;
                     } else {
-                        float2 g;
-                        g.x = __fmul_rn(f[i], inv);
-                        g.y = __fmul_rn(f[i + 1], inv);
-                        pair = __nv_cvt_float2_to_fp8x2(g, __NV_SATFINITE, __NV_E4M3);
+                        pair = e4m3x2(__fmul_rn(f[i], inv), __fmul_rn(f[i + 1], inv));
                     }
                     word |= (pair & 0xffffu) << (16 * p);
                 }
@@ -242,6 +251,35 @@ cudaError_t launch_layout_dispatch_quant(int T, int H, int k, int E, int R,
     // the layout kernel is the previous grid: x may be read early
     return launch_fp8<false>(T, H, k, x, slot_of, recv_q, recv_scales, T * k, err_word, stream,
                              true);
+}
+
+// The encoding of consecutive fp32 bit patterns first, first + 1, ...
+// (wrapping past 2^32 - 1), one code per input.
+__global__ void e4m3_bits_kernel(uint32_t first, uint32_t count, uint8_t *__restrict__ codes)
+{
+    // 64-bit index: a count near 2^32 must not wrap the loop
+    const uint64_t stride = 2ull * gridDim.x * blockDim.x;
+    for (uint64_t i = 2ull * (blockIdx.x * blockDim.x + threadIdx.x); i < count; i += stride) {
+        const float a = __uint_as_float((uint32_t)(first + i));
+        const float b = __uint_as_float((uint32_t)(first + i + 1));
+        const uint32_t pair = e4m3x2(a, b);
+        codes[i] = (uint8_t)(pair & 0xffu);
+        if (i + 1 < count)
+            codes[i + 1] = (uint8_t)(pair >> 8);
+    }
+}
+
+cudaError_t launch_e4m3_bits(uint32_t first, uint32_t count, uint8_t *codes, cudaStream_t stream)
+{
+    if (count == 0)
+        return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = ((int64_t)count / 2 + threads) / threads;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (blocks > cap)
+        blocks = cap;
+    e4m3_bits_kernel<<<(unsigned)blocks, threads, 0, stream>>>(first, count, codes);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -62,6 +62,9 @@ cudaError_t launch_layout_dispatch_quant(int T, int H, int k, int E, int R,
                                          void *workspace, uint32_t *err_word,
                                          cudaStream_t stream);
 
+// The quantised dispatch's channel encoding on consecutive fp32 bit patterns.
+cudaError_t launch_e4m3_bits(uint32_t first, uint32_t count, uint8_t *codes, cudaStream_t stream);
+
 cudaError_t launch_dispatch_fp8(int T, int H, int k, const void *x, const int32_t *slot_of,
                                 uint8_t *recv_q, float *recv_scales, uint32_t *err_word,
                                 cudaStream_t stream);

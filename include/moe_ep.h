@@ -527,6 +527,19 @@ MOE_API moe_status moe_read_error(uint32_t *err_word, int clear, cudaStream_t st
                           uint32_t *bits_out);
 
 /*
+ * moe_e4m3_encode_bits -- diagnostic: the channel encoding moe_dispatch_quant
+ * applies (after scaling by 448 / amax), on the fp32 values whose bit patterns
+ * are first, first + 1, ..., first + count - 1 (modulo 2^32): codes[i] =
+ * E4M3 code of that value, nearest-even, saturating to +-448, infinities to
+ * +-448.  The pages have no counterpart; the call exists so that the kernel's
+ * encoding can be checked against the format's definition on every fp32
+ * input.  codes: count device bytes.  NaN inputs give a NaN code whose sign
+ * is not specified.
+ */
+MOE_API moe_status moe_e4m3_encode_bits(uint32_t first, uint32_t count, uint8_t *codes,
+                                        cudaStream_t stream);
+
+/*
  * moe_layout_last_form -- diagnostic: which form of the layout kernel the most
  * recent moe_layout, moe_layout_dispatch, moe_layout_coalesced or
  * moe_layout_noalloc call made by this host thread launched.  The pages have
