@@ -49,6 +49,7 @@ SIGNATURES = {
     "moe_layout_last_form": ([], ctypes.c_int),
     "moe_e4m3_encode_bits": ([ctypes.c_uint32, ctypes.c_uint32, _P, _P], ctypes.c_int),
     "moe_ep_reorder": ([_I, _I, _I, _P, _I, _P, _P, _I, _P, _U32P, _P], ctypes.c_int),
+    "moe_ep_reorder_rows": ([_I, _I, _I, _P, _I, _P, _P, _I, _P, _U32P, _P], ctypes.c_int),
     "moe_combine_backward": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _U32P, _P], ctypes.c_int),
     "moe_dispatch_backward": ([_I, _I, _I, _P, _P, _P, _I, _U32P, _P], ctypes.c_int),
     "moe_layout_coalesced": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _U32P, _P],
@@ -569,7 +570,7 @@ __all__ = [
     "CoalescedLayout", "moe_layout_coalesced", "moe_dispatch_coalesced", "moe_dispatch_quant_coalesced",
     "moe_combine_coalesced",
     "moe_dispatch_combine_flagged", "moe_ep_reorder", "moe_layout_last_form",
-    "moe_e4m3_encode_bits", "LIB_PATH",
+    "moe_e4m3_encode_bits", "moe_ep_reorder_rows", "LIB_PATH",
     "SIGNATURES",
 ]
 
@@ -597,4 +598,33 @@ def moe_ep_reorder(src: torch.Tensor, recv_counts: torch.Tensor, *, to_source: b
                                MOE_EP_TO_SOURCE if to_source else MOE_EP_TO_EXPERT,
                                _ptr(local_expert_offsets), _ptr(err_word), _stream(stream)),
            "moe_ep_reorder")
+    return out
+
+
+def moe_ep_reorder_rows(src: torch.Tensor, recv_counts: torch.Tensor, *, to_source: bool = False,
+                        out: Optional[torch.Tensor] = None,
+                        local_expert_offsets: Optional[torch.Tensor] = None,
+                        err_word: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """moe_ep_reorder for rows of any contiguous payload (the first dimension
+    indexes rows; a row's size must be a multiple of 4 bytes)."""
+    if recv_counts.dim() != 2:
+        raise ValueError("recv_counts must be [W, El]")
+    W, El = recv_counts.shape
+    _want(recv_counts, "recv_counts", torch.int32)
+    if not src.is_cuda or not src.is_contiguous() or src.dim() < 1:
+        raise ValueError("src must be a contiguous CUDA tensor of rows")
+    rows = src.shape[0]
+    row_bytes = (src.numel() // rows if rows else int(torch.tensor(src.shape[1:]).prod())) * \
+        src.element_size()
+    if out is None:
+        out = torch.empty_like(src)
+    if out.shape != src.shape or out.dtype != src.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like src")
+    if local_expert_offsets is not None:
+        _want(local_expert_offsets, "local_expert_offsets", torch.int32, (El + 1,))
+    _check(_lib.moe_ep_reorder_rows(W, El, row_bytes, _ptr(recv_counts), rows, _ptr(src),
+                                    _ptr(out), MOE_EP_TO_SOURCE if to_source else
+                                    MOE_EP_TO_EXPERT, _ptr(local_expert_offsets),
+                                    _ptr(err_word), _stream(stream)), "moe_ep_reorder_rows")
     return out

@@ -381,7 +381,30 @@ moe_status moe_ep_reorder(int W, int El, int H, const int32_t *recv_counts, int 
     if (!aligned(src, 16) || !aligned(dst, 16) || !aligned(recv_counts, 4) ||
         !aligned(local_expert_offsets, 4) || !aligned(err_word, 4))
         return MOE_ERR_INVALID_ARG;
-    return from_cuda(moe::launch_ep_reorder(W, El, H, recv_counts, rows, src, dst,
+    return from_cuda(moe::launch_ep_reorder(W, El, 2 * (int64_t)H, recv_counts, rows, src, dst,
+                                            direction == MOE_EP_TO_SOURCE, local_expert_offsets,
+                                            err_word, stream));
+}
+
+moe_status moe_ep_reorder_rows(int W, int El, int row_bytes, const int32_t *recv_counts,
+                               int rows, const void *src, void *dst, int direction,
+                               int32_t *local_expert_offsets, uint32_t *err_word,
+                               cudaStream_t stream)
+{
+    if (W < 1 || El < 1 || row_bytes < 4 || row_bytes % 4 != 0 || rows < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (direction != MOE_EP_TO_EXPERT && direction != MOE_EP_TO_SOURCE)
+        return MOE_ERR_INVALID_ARG;
+    if ((int64_t)W * El > MOE_MAX_EXPERTS)
+        return MOE_ERR_UNSUPPORTED;
+    if (!recv_counts || (rows > 0 && (!src || !dst)))
+        return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && src == dst)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(src, 4) || !aligned(dst, 4) || !aligned(recv_counts, 4) ||
+        !aligned(local_expert_offsets, 4) || !aligned(err_word, 4))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_ep_reorder(W, El, row_bytes, recv_counts, rows, src, dst,
                                             direction == MOE_EP_TO_SOURCE, local_expert_offsets,
                                             err_word, stream));
 }

@@ -87,8 +87,8 @@ cudaError_t launch_combine_backward(int T, int H, int k, const void *dout, const
                                     const int32_t *slot_of, const float *topk_w, void *dy,
                                     float *dw, uint32_t *err_word, cudaStream_t stream);
 
-cudaError_t launch_ep_reorder(int W, int El, int H, const int32_t *recv_counts, int64_t rows,
-                              const void *src, void *dst, bool to_source,
+cudaError_t launch_ep_reorder(int W, int El, int64_t row_bytes, const int32_t *recv_counts,
+                              int64_t rows, const void *src, void *dst, bool to_source,
                               int32_t *local_expert_offsets, uint32_t *err_word,
                               cudaStream_t stream);
 

@@ -481,6 +481,20 @@ MOE_API moe_status moe_ep_reorder(int W, int El, int H, const int32_t *recv_coun
                                   cudaStream_t stream);
 
 /*
+ * moe_ep_reorder_rows -- moe_ep_reorder for rows of any payload: `row_bytes`
+ * bytes per row (a multiple of 4; src and dst 4-byte aligned, 16-byte aligned
+ * rows of a multiple of 16 bytes move as 16-byte vectors).  With the FP8
+ * dispatch across ranks (UBEP Table 3: W8A8) a receiver reorders the E4M3
+ * code rows (H bytes) and the scale rows (H / 128 fp32) with two calls on the
+ * same counts.  Same counts, directions, offsets and errors as
+ * moe_ep_reorder.
+ */
+MOE_API moe_status moe_ep_reorder_rows(int W, int El, int row_bytes, const int32_t *recv_counts,
+                                       int rows, const void *src, void *dst, int direction,
+                                       int32_t *local_expert_offsets, uint32_t *err_word,
+                                       cudaStream_t stream);
+
+/*
  * moe_layout_noalloc -- moe_layout for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a deployment convenience.
  *

@@ -43,6 +43,10 @@ class CpuOps:
     def dispatch(self, x, slot_of):
         return _bf16(oracle.dispatch(_bits(x), slot_of.numpy()))
 
+    def dispatch_quant(self, x, slot_of):
+        q, sc = oracle.dispatch_quant(_bits(x), slot_of.numpy())
+        return torch.from_numpy(q), torch.from_numpy(sc)
+
     def reorder(self, src, recv_counts, to_source, with_offsets):
         cnt = recv_counts.numpy().astype(np.int64)
         W, El = cnt.shape
@@ -53,7 +57,8 @@ class CpuOps:
             for el in range(El):
                 n = cnt[s, el]
                 perm[s_start[s, el]:s_start[s, el] + n] = e_start[s, el] + np.arange(n)
-        a = _bits(src)
+        bf = src.dtype == torch.bfloat16
+        a = _bits(src) if bf else src.numpy()
         out = np.empty_like(a)
         if to_source:
             out[:] = a[perm]
@@ -62,7 +67,7 @@ class CpuOps:
         offs = None
         if with_offsets:
             offs = torch.from_numpy(np.append(e_start[0], cnt.sum()).astype(np.int32))
-        return _bf16(out), offs
+        return (_bf16(out) if bf else torch.from_numpy(out)), offs
 
     def combine(self, y, slot_of, topk_w):
         return _bf16(oracle.combine(_bits(y), slot_of.numpy(), topk_w.numpy(), "bf16"))
@@ -72,7 +77,7 @@ def _inputs(W, T_per, H, k, E):
     return [random_case(500 + s, T_per[s], H, k, E, W) for s in range(W)]
 
 
-def _rank_main(rank, W, port, T_per, H, k, E, q):
+def _rank_main(rank, W, port, T_per, H, k, E, q, quant=False):
     import torch.distributed as dist
     from combine_layout_moe_gb300 import ep
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
@@ -81,11 +86,13 @@ def _rank_main(rank, W, port, T_per, H, k, E, q):
         ins = _inputs(W, T_per, H, k, E)
         me = ins[rank]
         epl = ep.ExpertParallel(E, ops=CpuOps())
-        recv, offs, handle = epl.dispatch(_bf16(me.x), torch.from_numpy(me.topk_idx))
+        recv, offs, handle = epl.dispatch(_bf16(me.x), torch.from_numpy(me.topk_idx), quant=quant)
+        rows = recv[0].shape[0] if quant else recv.shape[0]
         # an expert that is not the identity: each receiver's own rows
-        y = _bf16(expert_output(recv.shape[0], H, seed=900 + rank))
+        y = _bf16(expert_output(rows, H, seed=900 + rank))
         out = epl.combine(y, handle, torch.from_numpy(me.topk_w))
-        q.put((rank, _bits(recv), offs.numpy(), _bits(out), handle[1].recv_splits,
+        got = (recv[0].numpy(), recv[1].numpy()) if quant else _bits(recv)
+        q.put((rank, got, offs.numpy(), _bits(out), handle[1].recv_splits,
                handle[0].send_splits))
     except Exception as e:  # reported to the parent, which fails the test
         q.put((rank, repr(e)))
@@ -160,3 +167,45 @@ def test_virtual_step_on_cpu_stand_ins_matches_oracle():
     for d in range(W):
         assert np.array_equal(_bits(recv[d]).reshape(o_recv[d].shape), o_recv[d])
         assert np.array_equal(_bits(outs[d]).reshape(o_out[d].shape), o_out[d])
+
+
+@pytest.mark.parametrize("W,T_per,H,k,E", [(2, [37, 23], 256, 2, 4), (3, [11, 29, 0], 128, 8, 6)])
+def test_fp8_exchange_over_gloo_matches_oracle(W, T_per, H, k, E):
+    """The FP8 dispatch across ranks (UBEP Table 3: W8A8): each receiver gets
+    the E4M3 codes and fp32 scales of the tokens routed to it, in the receive
+    order of the bf16 path; the combine's return path is bf16 as before."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _port()
+    procs = [ctx.Process(target=_rank_main, args=(r, W, port, T_per, H, k, E, q, True))
+             for r in range(W)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(W):
+        item = q.get(timeout=120)
+        res[item[0]] = item
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(W):
+        assert len(res[r]) > 2, res[r][1]
+    ins = _inputs(W, T_per, H, k, E)
+    counts, recv, src = oracle.ep_dispatch([w.topk_idx for w in ins], [w.x for w in ins], E)
+    # each token's codes and scales: the oracle's FP8 dispatch of the token
+    # alone (one slot per token); a received row holds its source token's
+    tq, ts = [], []
+    for w in ins:
+        a, b = oracle.dispatch_quant(w.x, np.arange(w.T, dtype=np.int32).reshape(w.T, 1))
+        tq.append(a)
+        ts.append(b)
+    tq, ts = np.concatenate(tq), np.concatenate(ts)
+    ys = [expert_output(len(recv[d]), H, seed=900 + d) for d in range(W)]
+    outs = oracle.ep_combine([w.topk_idx for w in ins], [w.topk_w for w in ins], ys, E)
+    for d in range(W):
+        _, (g_q, g_s), g_offs, g_out, _, _ = res[d]
+        tok = src[d] // k
+        assert np.array_equal(g_q, tq[tok])
+        assert np.array_equal(g_s, ts[tok])
+        assert np.array_equal(g_offs, np.concatenate([[0], np.cumsum(counts[d].sum(axis=0))]))
+        assert np.array_equal(g_out.reshape(outs[d].shape), outs[d])

@@ -118,3 +118,74 @@ def test_reorder_empty():
                            local_expert_offsets=offs)
     torch.cuda.synchronize()
     assert out.shape == (0, 8) and offs.cpu().tolist() == [0, 0, 0]
+
+
+@pytest.mark.parametrize("name,W,T", [("dsv3_prefill", 8, 128), ("glm45_air", 4, 256),
+                                      ("mixtral", 2, 1024)])
+def test_virtual_ranks_fp8_dispatch(name, W, T):
+    """The FP8 dispatch across ranks: every receiver holds the E4M3 codes and
+    fp32 scales of its tokens in the bf16 path's receive order (codes and
+    scales reordered as rows of H and H / 128 * 4 bytes); the return path is
+    bf16."""
+    import combine_layout_moe_gb300 as m
+    from combine_layout_moe_gb300 import ep
+    ins = [make_workload(name, seed=s, T=T) for s in range(W)]
+    E, H, k = ins[0].E, ins[0].H, ins[0].k
+    err = m.new_error_word()
+    ys = {}
+
+    def expert(recv, offs):
+        d = len(ys)
+        ys[d] = expert_output(recv[0].shape[0], H, seed=400 + d)
+        return bf16_dev(ys[d])
+
+    recv, offs, outs = ep.virtual_step([bf16_dev(w.x) for w in ins],
+                                       [torch.from_numpy(w.topk_idx).cuda() for w in ins],
+                                       [torch.from_numpy(w.topk_w).cuda() for w in ins], E,
+                                       expert=expert, ops=ep.LibraryOps(err), quant=True)
+    torch.cuda.synchronize()
+    assert m.moe_read_error(err) == 0
+    counts, _, src = oracle.ep_dispatch([w.topk_idx for w in ins], [w.x for w in ins], E)
+    tq = np.concatenate([oracle.dispatch_quant(w.x, np.arange(w.T, dtype=np.int32)[:, None])[0]
+                         for w in ins])
+    ts = np.concatenate([oracle.dispatch_quant(w.x, np.arange(w.T, dtype=np.int32)[:, None])[1]
+                         for w in ins])
+    o_out = oracle.ep_combine([w.topk_idx for w in ins], [w.topk_w for w in ins],
+                              [ys[d] for d in range(W)], E)
+    for d in range(W):
+        tok = src[d] // k
+        assert np.array_equal(recv[d][0].cpu().numpy(), tq[tok]), d
+        assert np.array_equal(recv[d][1].cpu().numpy(), ts[tok]), d
+        want = np.concatenate([[0], np.cumsum(counts[d].sum(axis=0))])
+        assert np.array_equal(offs[d].cpu().numpy(), want), d
+        assert np.array_equal(bits(outs[d]).reshape(o_out[d].shape), o_out[d]), d
+
+
+@pytest.mark.parametrize("shape,dtype", [((37, 1), torch.float32), ((50, 56), torch.float32),
+                                         ((30, 3), torch.float32), ((64, 7168), torch.uint8),
+                                         ((20, 12), torch.int32)])
+def test_reorder_rows_of_any_width(shape, dtype):
+    """moe_ep_reorder_rows on 4-byte rows (one fp32 scale), scale rows of a
+    7168-channel token, 12-byte rows (4-byte copies), FP8 code rows, and
+    48-byte rows: round trip and the expert-major placement."""
+    import combine_layout_moe_gb300 as m
+    W, El = 3, 2
+    rng = np.random.default_rng(3)
+    cnt = rng.integers(0, 8, size=(W, El)).astype(np.int32)
+    rows = int(cnt.sum())
+    full = (rows,) + shape[1:]
+    src = torch.from_numpy(rng.integers(0, 100, size=full).astype(
+        {torch.float32: np.float32, torch.uint8: np.uint8, torch.int32: np.int32}[dtype])).cuda()
+    rc = torch.from_numpy(cnt).cuda()
+    fwd = m.moe_ep_reorder_rows(src, rc)
+    back = m.moe_ep_reorder_rows(fwd, rc, to_source=True)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    s_start = np.concatenate([[0], np.cumsum(cnt.reshape(-1))])
+    e_start = np.concatenate([[0], np.cumsum(cnt.T.reshape(-1))])
+    a, b = src.cpu().numpy(), fwd.cpu().numpy()
+    for s in range(W):
+        for el in range(El):
+            n = cnt[s, el]
+            assert np.array_equal(b[e_start[el * W + s]:e_start[el * W + s] + n],
+                                  a[s_start[s * El + el]:s_start[s * El + el] + n])
