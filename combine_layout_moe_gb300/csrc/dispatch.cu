@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tma.cuh"
+#include "sched.cuh"
 
 namespace moe {
 
@@ -27,17 +28,35 @@ namespace moe {
 #endif
 constexpr int DB_STAGES = MOE_DB_STAGES;  // row chunks in flight per pipe
 constexpr int DB_CHUNK = MOE_DB_CHUNK;    // bytes per bulk copy (last chunk of a row may be shorter)
+#ifndef MOE_DB_STATIC_PCT
+#define MOE_DB_STATIC_PCT 50
+#endif
+#ifndef MOE_DB_GRAB
+#define MOE_DB_GRAB 1
+#endif
+#ifndef MOE_DB_DYN_MIN
+#define MOE_DB_DYN_MIN 8
+#endif
+constexpr int DB_STATIC_PCT = MOE_DB_STATIC_PCT;  // share of the units split statically
+constexpr int DB_GRAB = MOE_DB_GRAB;              // units per draw from the pool
+constexpr int DB_DYN_MIN = MOE_DB_DYN_MIN;        // below this many units per CTA only the
+                                                  // remainder of an equal split is drawn
 static_assert(DB_STAGES >= 2 && DB_STAGES <= 16, "stage ring size");
 
 // bf16 dispatch through bulk copies.  Each CTA is one warp driving one
-// pipeline over a contiguous range of units (unit = token t, chunk c of its
-// row): lane 0 loads the chunk into a ring of shared-memory stages with one
-// cp.async.bulk (completion on the stage's mbarrier); once it has landed,
-// lanes 0..k-1 each store it to their destination row with one shared ->
-// global cp.async.bulk.  A stage is refilled only after every lane's stores
-// from it have finished reading shared memory (bulk async-group accounting:
-// every lane commits one group per unit, possibly empty).  The row is read
-// from HBM once and written k times with no per-element instructions.
+// pipeline over units (unit = token t, chunk c of its row): lane 0 loads the
+// chunk into a ring of shared-memory stages with one cp.async.bulk
+// (completion on the stage's mbarrier); once it has landed, lanes 0..k-1 each
+// store it to their destination row with one shared -> global cp.async.bulk.
+// A stage is refilled only after every lane's stores from it have finished
+// reading shared memory (bulk async-group accounting: every lane commits one
+// group per unit, possibly empty).  The row is read from HBM once and written
+// k times with no per-element instructions.
+//
+// Units: each CTA first takes `per_cta` consecutive units of its own, then
+// draws `grab` consecutive units at a time from the pool of the rest (the
+// scheduling slot `sched_slot` of the launch; see sched.cuh).  The stage ring
+// records the unit each stage holds.
 //
 // COAL: rows go to the rank-coalesced buffer (one row per token and distinct
 // destination rank).  slot_of is then the coalesced row map, where every slot
@@ -48,14 +67,18 @@ static_assert(DB_STAGES >= 2 && DB_STAGES <= 16, "stage ring size");
 // previous grid.  Only for a launch whose previous grid is this library's
 // layout kernel: that kernel lets dependents launch only after its own wait,
 // so x (written before the layout) is final, and only slot_of is not.
+__device__ SchedSlot g_dispatch_sched[SCHED_SLOTS];
+static std::atomic<unsigned> g_dispatch_seq{0};
+
 template <bool COAL>
 __global__ void __launch_bounds__(32)
     dispatch_bulk_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ slot_of,
                          uint8_t *__restrict__ recv, int T, int k, int64_t rowbytes, int CH,
-                         int nchunks, int64_t units, int rows, int prefetch_x,
-                         uint32_t *err_word)
+                         int nchunks, int64_t units, int64_t per_cta, int grab, int sched_slot,
+                         int rows, int prefetch_x, uint32_t *err_word)
 {
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int64_t stage_unit[DB_STAGES];
     const uint32_t bars = smem_addr(smem);
     const uint32_t stages = bars + 128;
     auto full = [&](int s) { return bars + 8u * s; };
@@ -68,44 +91,74 @@ __global__ void __launch_bounds__(32)
     }
     __syncwarp();
 
-    const int64_t u0 = units * blockIdx.x / gridDim.x;
-    const int64_t u1 = units * (blockIdx.x + 1) / gridDim.x;
-    const int64_t nloc = u1 - u0;
+    // the unit source (warp-uniform): this CTA's range, then draws from the
+    // pool [per_cta * gridDim.x, units); a draw is requested as soon as the
+    // current range is used up, so it travels while the last unit loads
+    SchedSlot *sched = g_dispatch_sched + sched_slot;
+    const int64_t pool0 = per_cta * gridDim.x;
+    int64_t r_cur = per_cta * blockIdx.x, r_end = r_cur + per_cta;
+    unsigned long long drawn = 0;  // lane 0: the pending draw's pool offset
+    bool pending = false, dry = pool0 >= units;
+    auto request = [&]() {
+        if (lane == 0)
+            drawn = atomicAdd(&sched->taken, (unsigned long long)grab);
+        pending = true;
+    };
+    auto next_unit = [&]() -> int64_t {
+        if (r_cur == r_end) {
+            if (dry)
+                return -1;
+            if (!pending)
+                request();
+            const int64_t v = pool0 + (int64_t)__shfl_sync(FULL_MASK, drawn, 0);
+            pending = false;
+            if (v >= units) {
+                dry = true;
+                return -1;
+            }
+            r_cur = v;
+            r_end = min(v + (int64_t)grab, units);
+        }
+        const int64_t u = r_cur++;
+        if (r_cur == r_end && !dry)
+            request();
+        return u;
+    };
 
-    // load cursor (lane 0 issues loads in unit order)
-    int64_t lt = u0 / nchunks;
-    int lc = (int)(u0 - lt * nchunks);
+    // load side (the whole warp runs it; lane 0 issues the copy)
     int64_t loaded = 0;
+    bool more = true;
     auto issue_load = [&]() {
+        const int64_t u = next_unit();
+        if (u < 0) {
+            more = false;
+            return;
+        }
         const int s = (int)(loaded % DB_STAGES);
+        const int64_t lt = u / nchunks;
+        const int lc = (int)(u - lt * nchunks);
         const uint32_t cb = (uint32_t)min((int64_t)CH, rowbytes - (int64_t)lc * CH);
         if (lane == 0) {
+            stage_unit[s] = u;
             mbar_arrive_expect_tx(full(s), cb);
             bulk_g2s(stages + (uint32_t)s * CH, x + lt * rowbytes + (int64_t)lc * CH, cb, full(s));
         }
         ++loaded;
-        if (++lc == nchunks) {
-            lc = 0;
-            ++lt;
-        }
+        __syncwarp();  // stage_unit[s] is visible to every lane
     };
     if (prefetch_x) {
-        while (loaded < nloc && loaded < DB_STAGES)
+        while (more && loaded < DB_STAGES)
             issue_load();
     }
     wait_prior_grid();
     allow_next_grid();
-    if (nloc <= 0)
-        return;
-    while (loaded < nloc && loaded < DB_STAGES)
+    while (more && loaded < DB_STAGES)
         issue_load();
 
-    // store cursor
-    int64_t t = u0 / nchunks;
-    int c = (int)(u0 - t * nchunks);
+    // store side: a lane stores its slot's row unless (COAL) a lower slot of
+    // the token names the same row; the slots of the next unit's token are
+    // requested one unit ahead
     const bool kl = lane < k;
-    // a lane stores its slot's row unless (COAL) a lower slot of the token
-    // names the same row
     const unsigned kmask = k >= 32 ? FULL_MASK : (1u << k) - 1u;
     auto first_of_row = [&](int32_t v) {
         if (!COAL)
@@ -113,20 +166,28 @@ __global__ void __launch_bounds__(32)
         const unsigned same = __match_any_sync(FULL_MASK, v) & kmask;
         return kl && (same & lanemask_lt()) == 0;
     };
-    int32_t cur = kl ? ld_nc_s32(slot_of + t * k + lane) : 0;
-    int32_t nxt = kl && t + 1 < T ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
-    bool st = first_of_row(cur);
+    int64_t cur_t = -1, nxt_t = -1;
+    int32_t cur = 0, nxt = 0;
+    bool st = false;
     int64_t n = 0;
     bool timed_out = false;
-    for (; n < nloc; ++n) {
-        if (n > 0 && ++c == nchunks) {
-            c = 0;
-            ++t;
-            cur = nxt;
-            nxt = kl && t + 1 < T ? ld_nc_s32(slot_of + (t + 1) * k + lane) : 0;
+    for (; n < loaded; ++n) {
+        const int s = (int)(n % DB_STAGES);
+        const int64_t u = stage_unit[s];
+        const int64_t t = u / nchunks;
+        const int c = (int)(u - t * nchunks);
+        if (t != cur_t) {
+            cur = t == nxt_t ? nxt : kl ? ld_nc_s32(slot_of + t * k + lane) : 0;
+            cur_t = t;
             st = first_of_row(cur);
         }
-        const int s = (int)(n % DB_STAGES);
+        if (n + 1 < loaded) {
+            const int64_t tn = stage_unit[(n + 1) % DB_STAGES] / nchunks;
+            if (tn != cur_t && tn != nxt_t) {
+                nxt = kl ? ld_nc_s32(slot_of + tn * k + lane) : 0;
+                nxt_t = tn;
+            }
+        }
         if (!mbar_wait(full(s), (uint32_t)(n / DB_STAGES) & 1)) {
             timed_out = true;
             break;
@@ -141,7 +202,7 @@ __global__ void __launch_bounds__(32)
         }
         bulk_commit();
         // refill the stage unit n-1 used with the next unit to load
-        if (n >= 1 && loaded < nloc) {
+        if (n >= 1 && more) {
             bulk_wait_read<1>();
             __syncwarp();
             issue_load();
@@ -154,6 +215,8 @@ __global__ void __launch_bounds__(32)
             (void)mbar_wait(full((int)(m % DB_STAGES)), (uint32_t)(m / DB_STAGES) & 1);
     }
     bulk_wait_all();
+    if (lane == 0)
+        sched_finish(sched);
 }
 
 constexpr int DISPATCH_THREADS = 256;
@@ -223,9 +286,12 @@ static cudaError_t launch_dispatch_bulk(int T, int H, int k, const void *x,
         per_sm = 1;
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const int64_t g = units < cap ? units : cap;
+    const int64_t even = units / g;
+    const int64_t per_cta = even >= DB_DYN_MIN ? units * DB_STATIC_PCT / 100 / g : even;
     return launch_pdl(dispatch_bulk_kernel<COAL>, dim3((unsigned)g), dim3(32), smem, stream,
                       static_cast<const uint8_t *>(x), slot_of, static_cast<uint8_t *>(recv), T, k,
-                      rowbytes, CH, nchunks, units, rows, prefetch_x ? 1 : 0, err_word);
+                      rowbytes, CH, nchunks, units, per_cta, DB_GRAB,
+                      next_sched_slot(g_dispatch_seq), rows, prefetch_x ? 1 : 0, err_word);
 }
 
 cudaError_t launch_dispatch_coalesced(int T, int H, int k, const void *x, const int32_t *crow,

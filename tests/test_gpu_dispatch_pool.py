@@ -1,0 +1,105 @@
+"""The bulk dispatch's shared pool of units (a CTA takes a fixed share of the
+units, then draws the rest from a counter of the launch): every unit is copied
+exactly once whichever CTA draws it, on shapes that take the fixed share by
+percentage and by the whole units of an equal split; the counter's slot is
+clean again for the next launch, for the replays of a captured graph, and
+after more launches than there are slots, from two streams at once.  Each
+receive buffer is compared bit for bit with the oracle's dispatch."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads.gen import random_case
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _case(seed, T, H, k, E):
+    w = random_case(seed, T, H, k, E, 1)
+    slot_of = oracle.layout(w.topk_idx, E, 1)[3]
+    return w, slot_of
+
+
+# (T, H, k, E): 8192 one-chunk rows (about 9 units per CTA: half of them drawn);
+# 3000 rows of two unequal chunks (about 6.6 units per CTA: the remainder of
+# an equal split drawn); 911 single units (fewer units than CTAs could run)
+SHAPES = [(8192, 256, 4, 32), (3000, 7168, 3, 24), (911, 64, 2, 8)]
+
+
+@pytest.mark.parametrize("T,H,k,E", SHAPES)
+def test_every_unit_copied_once(T, H, k, E):
+    import combine_layout_moe_gb300 as m
+    w, slot_of = _case(31, T, H, k, E)
+    so = torch.from_numpy(slot_of).cuda()
+    err = m.new_error_word()
+    recv = torch.empty((T * k, H), dtype=torch.bfloat16, device="cuda")
+    for rep in range(4):
+        x = w.x if rep % 2 == 0 else w.x ^ np.uint16(0x0100 * (rep + 1))
+        recv.fill_(float("nan"))
+        m.moe_dispatch(_bf16(x), so, recv=recv, err_word=err)
+        torch.cuda.synchronize()
+        assert m.moe_read_error(err) == 0
+        assert np.array_equal(_bits(recv).reshape(T * k, H), oracle.dispatch(x, slot_of)), rep
+
+
+def test_graph_replays_reuse_a_clean_slot():
+    import combine_layout_moe_gb300 as m
+    T, H, k, E = SHAPES[0]
+    w, slot_of = _case(32, T, H, k, E)
+    so = torch.from_numpy(slot_of).cuda()
+    err = m.new_error_word()
+    x = _bf16(w.x)
+    recv = torch.empty((T * k, H), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        m.moe_dispatch(x, so, recv=recv, err_word=err)   # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        m.moe_dispatch(x, so, recv=recv, err_word=err)
+    for rep in range(4):
+        xr = w.x ^ np.uint16(0x0010 * (rep + 1))
+        x.copy_(_bf16(xr))
+        recv.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert m.moe_read_error(err) == 0
+        assert np.array_equal(_bits(recv).reshape(T * k, H), oracle.dispatch(xr, slot_of)), rep
+
+
+def test_more_launches_than_slots_on_two_streams():
+    """1100 launches per stream (the slot table holds 1024), the two streams'
+    launches free to overlap; each stream's buffer is checked every 100
+    launches and at the end."""
+    import combine_layout_moe_gb300 as m
+    T, H, k, E = 2048, 64, 2, 8
+    cases = [_case(40 + i, T, H, k, E) for i in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    errs = [m.new_error_word() for _ in range(2)]
+    xs = [_bf16(w.x) for w, _ in cases]
+    sos = [torch.from_numpy(so).cuda() for _, so in cases]
+    recvs = [torch.empty((T * k, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    want = [oracle.dispatch(w.x, so) for w, so in cases]
+    torch.cuda.synchronize()
+    for it in range(1100):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                if it % 100 == 99:
+                    recvs[i].fill_(float("nan"))
+                m.moe_dispatch(xs[i], sos[i], recv=recvs[i], err_word=errs[i], stream=streams[i])
+        if it % 100 == 99:
+            torch.cuda.synchronize()
+            for i in range(2):
+                assert m.moe_read_error(errs[i]) == 0
+                assert np.array_equal(_bits(recvs[i]).reshape(T * k, H), want[i]), (it, i)
