@@ -10,11 +10,18 @@
 // GPU design: a warp item is one token and 2U blocks of 128 channels; each
 // half-warp owns a block (16 lanes x 8 channels, U 16-byte vectors of x in
 // flight per lane), reduces its amax with xor-shuffles, and stores 8-byte code
-// words and one fp32 scale per block to every destination row.
+// words and one fp32 scale per block to every destination row.  When the
+// items take more than QUANT_DYN_MIN_ROUNDS rounds of the resident warps, the
+// warps take QUANT_STATIC_PCT percent of them in interleaved rounds (warp w:
+// items w, w + warps, ...), then draw the rest from the launch's pool
+// (sched.cuh), the next draw requested while the current items are
+// processed; a draw takes enough items to cover SCHED_DRAW_BYTES of traffic,
+// which keeps the draws on the pool's one counter far apart.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "launch.h"
+#include "sched.cuh"
 
 namespace moe {
 
@@ -40,18 +47,31 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
 #define MOE_QUANT_U 4
 #endif
 constexpr int QUANT_U = MOE_QUANT_U;
+#ifndef MOE_QUANT_STATIC_PCT
+#define MOE_QUANT_STATIC_PCT 50
+#endif
+#ifndef MOE_QUANT_DYN_MIN_ROUNDS
+#define MOE_QUANT_DYN_MIN_ROUNDS 4
+#endif
+constexpr int QUANT_STATIC_PCT = MOE_QUANT_STATIC_PCT;
+constexpr int QUANT_DYN_MIN_ROUNDS = MOE_QUANT_DYN_MIN_ROUNDS;
+__device__ SchedSlot g_quant_sched[SCHED_SLOTS];
+static std::atomic<unsigned> g_quant_seq{0};
 
 // FP8: each half-warp owns one 128-channel block (16 lanes x 8 channels).
 // The amax is reduced with xor-shuffles inside the half-warp; scale and
 // reciprocal are each one correctly rounded fp32 division; each channel is one
 // rounded fp32 multiply followed by a saturating nearest-even E4M3 conversion.
-template <int U, bool COAL>
+template <int U, bool COAL, bool POOL>
 __global__ void __launch_bounds__(QUANT_THREADS)
     dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
                         uint8_t *__restrict__ recv_q, float *__restrict__ recv_scales, int k,
-                        int H, int groups, int64_t items, int N, int prefetch_x,
-                        uint32_t *err_word)
+                        int H, int groups, int64_t items, int64_t pool_from, int grab,
+                        int sched_slot, int N, int prefetch_x, uint32_t *err_word)
 {
+    // POOL: items from pool_from on are drawn; else every item is taken in
+    // interleaved rounds and the pool code is compiled out
+    const int64_t static_items = POOL ? pool_from : items;
     // prefetch_x: the first item's x is loaded and quantised before waiting
     // for the previous grid, and only the slot map and the stores wait.  Only
     // for a launch whose previous grid is this library's layout kernel: that
@@ -66,8 +86,44 @@ __global__ void __launch_bounds__(QUANT_THREADS)
     const int C = H >> 3;    // 16-byte vectors per row
     const int B = H >> 7;    // 128-channel blocks per row
     const int64_t nwarps = (int64_t)gridDim.x * (QUANT_THREADS / 32);
-    for (int64_t it = (int64_t)blockIdx.x * (QUANT_THREADS / 32) + (threadIdx.x >> 5);
-         it < items; it += nwarps) {
+    // the item source (warp-uniform): interleaved rounds below static_items,
+    // then ranges drawn from the pool [static_items, items)
+    SchedSlot *sched = g_quant_sched + sched_slot;
+    unsigned long long drawn = 0;  // lane 0: the pending draw's pool offset
+    bool pending = false;
+    int64_t d_end = 0;
+    auto request = [&]() {
+        if (lane == 0)
+            drawn = atomicAdd(&sched->taken, (unsigned long long)grab);
+        pending = true;
+    };
+    auto draw = [&]() -> int64_t {
+        if (!pending)
+            request();
+        const int64_t v = static_items + (int64_t)__shfl_sync(FULL_MASK, drawn, 0);
+        pending = false;
+        if (v >= items)
+            return -1;
+        d_end = min(v + (int64_t)grab, items);
+        return v;
+    };
+    auto next_item = [&](int64_t it) -> int64_t {
+        if (it < static_items) {
+            if (it + nwarps < static_items)
+                return it + nwarps;
+        } else if (it + 1 < d_end) {
+            return it + 1;
+        }
+        return static_items < items ? draw() : -1;
+    };
+    int64_t it0 = (int64_t)blockIdx.x * (QUANT_THREADS / 32) + (threadIdx.x >> 5);
+    if (it0 >= static_items)
+        it0 = static_items < items ? draw() : -1;
+    for (int64_t it = it0; it >= 0; it = next_item(it)) {
+        // the next draw travels while this item is processed
+        if (!pending && (it >= static_items ? it + 1 >= d_end : it + nwarps >= static_items) &&
+            static_items < items)
+            request();
         const int64_t t = it / groups;
         const int c0 = (int)(it - t * groups) * (32 * U) + lane;
         const uint4 *src = x + t * C;
@@ -168,6 +224,11 @@ __global__ void __launch_bounds__(QUANT_THREADS)
         wait_prior_grid();
         allow_next_grid();
     }
+    if (static_items < items) {  // the same for every CTA
+        __syncthreads();         // every draw of this CTA is done
+        if (threadIdx.x == 0)
+            sched_finish(sched);
+    }
 }
 
 template <int U, bool COAL>
@@ -178,11 +239,24 @@ static cudaError_t launch_fp8_u(int T, int H, int k, const void *x, const int32_
     const int C = H / 8;
     const int groups = (C + 32 * U - 1) / (32 * U);
     const int64_t items = (int64_t)T * groups;
-    auto kern = dispatch_fp8_kernel<U, COAL>;
-    const int grid = warp_item_grid((const void *)kern, QUANT_THREADS, 0, items);
-    return launch_pdl(kern, dim3(grid), dim3(QUANT_THREADS), 0, stream,
-                      static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H, groups,
-                      items, rows, prefetch_x ? 1 : 0, err_word);
+    const int grid = warp_item_grid((const void *)dispatch_fp8_kernel<U, COAL, true>,
+                                    QUANT_THREADS, 0, items);
+    const int64_t warps = (int64_t)grid * (QUANT_THREADS / 32);
+    const int64_t rounds = (items + warps - 1) / warps;
+    // an item: 2U blocks of 128 channels read once, codes and scales written k times
+    const int64_t item_bytes = (int64_t)U * 256 * 2 + (int64_t)k * U * (256 + 8);
+    if (rounds > QUANT_DYN_MIN_ROUNDS) {
+        const int64_t pool_from = items * QUANT_STATIC_PCT / 100 / warps * warps;
+        return launch_pdl(dispatch_fp8_kernel<U, COAL, true>, dim3(grid), dim3(QUANT_THREADS),
+                          0, stream, static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales,
+                          k, H, groups, items, pool_from, sched_grab(item_bytes),
+                          next_sched_slot(g_quant_seq), rows, prefetch_x ? 1 : 0, err_word);
+    }
+    const int grid_s = warp_item_grid((const void *)dispatch_fp8_kernel<U, COAL, false>,
+                                      QUANT_THREADS, 0, items);
+    return launch_pdl(dispatch_fp8_kernel<U, COAL, false>, dim3(grid_s), dim3(QUANT_THREADS), 0,
+                      stream, static_cast<const uint4 *>(x), slot_of, recv_q, recv_scales, k, H,
+                      groups, items, items, 1, 0, rows, prefetch_x ? 1 : 0, err_word);
 }
 
 // Rounds of warp items the busiest warp runs, times the blocks per item: the
@@ -192,7 +266,7 @@ static int64_t fp8_rounds(int T, int H)
 {
     const int C = H / 8;
     const int64_t items = (int64_t)T * ((C + 32 * U - 1) / (32 * U));
-    auto kern = dispatch_fp8_kernel<U, COAL>;
+    auto kern = dispatch_fp8_kernel<U, COAL, false>;
     const int64_t warps = (int64_t)warp_item_grid((const void *)kern, QUANT_THREADS, 0,
                                                   items) * (QUANT_THREADS / 32);
     return (items + warps - 1) / warps * U;

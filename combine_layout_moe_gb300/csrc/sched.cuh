@@ -44,6 +44,19 @@ __device__ __forceinline__ void sched_finish(SchedSlot *s)
     }
 }
 
+// Host: units per draw so that each draw covers at least SCHED_DRAW_BYTES of
+// the launch's HBM traffic.  Draws on one counter are serialised where the
+// counter lives; at this spacing a launch moving bytes near the HBM's rate
+// asks for one draw every few nanoseconds at most, well inside what the
+// counter sustains (measured on one GB300: one-item draws of 4 KB items on
+// 65536 tokens slowed the FP8 dispatch from 206 to 253 us).
+constexpr int64_t SCHED_DRAW_BYTES = 16384;
+inline int sched_grab(int64_t unit_bytes)
+{
+    const int64_t g = (SCHED_DRAW_BYTES + unit_bytes - 1) / (unit_bytes > 0 ? unit_bytes : 1);
+    return (int)(g < 1 ? 1 : g);
+}
+
 // Host: the slot for the next launch of one kernel family.
 inline int next_sched_slot(std::atomic<unsigned> &seq)
 {

@@ -1,10 +1,11 @@
-"""The bulk dispatch's shared pool of units (a CTA takes a fixed share of the
-units, then draws the rest from a counter of the launch): every unit is copied
-exactly once whichever CTA draws it, on shapes that take the fixed share by
-percentage and by the whole units of an equal split; the counter's slot is
-clean again for the next launch, for the replays of a captured graph, and
-after more launches than there are slots, from two streams at once.  Each
-receive buffer is compared bit for bit with the oracle's dispatch."""
+"""The dispatch kernels' shared pool of work (a CTA or warp takes a fixed
+share, then draws the rest from a counter of the launch): every unit is copied
+(and, FP8, every item quantised) exactly once whichever CTA or warp draws it,
+on shapes that take the fixed share by percentage and by the whole units of
+an equal split; the counter's slot is clean again for the next launch, for
+the replays of a captured graph, and after more launches than there are
+slots, from two streams at once.  Each receive buffer is compared bit for bit
+with the oracle's dispatch."""
 import numpy as np
 import pytest
 import torch
@@ -103,3 +104,58 @@ def test_more_launches_than_slots_on_two_streams():
             for i in range(2):
                 assert m.moe_read_error(errs[i]) == 0
                 assert np.array_equal(_bits(recvs[i]).reshape(T * k, H), want[i]), (it, i)
+
+
+# FP8 (T, H, k, E): 20000 tokens of one 256-channel item (5 rounds of the
+# resident warps: the pool); 6000 tokens of 7168 channels (about 9 rounds)
+FP8_SHAPES = [(20000, 256, 8, 64), (6000, 7168, 3, 24)]
+
+
+@pytest.mark.parametrize("T,H,k,E", FP8_SHAPES)
+def test_fp8_every_item_once(T, H, k, E):
+    import combine_layout_moe_gb300 as m
+    w, slot_of = _case(51, T, H, k, E)
+    so = torch.from_numpy(slot_of).cuda()
+    err = m.new_error_word()
+    q = torch.empty((T * k, H), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((T * k, H // 128), dtype=torch.float32, device="cuda")
+    for rep in range(3):
+        x = w.x if rep == 0 else w.x ^ np.uint16(0x0010 * rep)
+        q.fill_(0x5A)
+        sc.fill_(-1.0)
+        m.moe_dispatch_quant(_bf16(x), so, recv_q=q, recv_scales=sc, err_word=err)
+        torch.cuda.synchronize()
+        assert m.moe_read_error(err) == 0
+        rq, rs = oracle.dispatch_quant(x, slot_of)
+        assert np.array_equal(q.cpu().numpy(), rq), rep
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), rs.view(np.uint32)), rep
+
+
+def test_fp8_graph_replays_reuse_a_clean_slot():
+    import combine_layout_moe_gb300 as m
+    T, H, k, E = FP8_SHAPES[0]
+    w, slot_of = _case(52, T, H, k, E)
+    so = torch.from_numpy(slot_of).cuda()
+    err = m.new_error_word()
+    x = _bf16(w.x)
+    q = torch.empty((T * k, H), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((T * k, H // 128), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        m.moe_dispatch_quant(x, so, recv_q=q, recv_scales=sc, err_word=err)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        m.moe_dispatch_quant(x, so, recv_q=q, recv_scales=sc, err_word=err)
+    for rep in range(3):
+        xr = w.x ^ np.uint16(0x0020 * (rep + 1))
+        x.copy_(_bf16(xr))
+        q.fill_(0x5A)
+        g.replay()
+        torch.cuda.synchronize()
+        assert m.moe_read_error(err) == 0
+        rq, rs = oracle.dispatch_quant(xr, slot_of)
+        assert np.array_equal(q.cpu().numpy(), rq), rep
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), rs.view(np.uint32)), rep
