@@ -39,8 +39,7 @@ constexpr int DB_CHUNK = MOE_DB_CHUNK;    // bytes per bulk copy (last chunk of 
 #endif
 constexpr int DB_STATIC_PCT = MOE_DB_STATIC_PCT;  // share of the units split statically
 constexpr int DB_GRAB = MOE_DB_GRAB;              // units per draw from the pool
-constexpr int DB_DYN_MIN = MOE_DB_DYN_MIN;        // below this many units per CTA only the
-                                                  // remainder of an equal split is drawn
+constexpr int DB_DYN_MIN = MOE_DB_DYN_MIN;        // below this many units per CTA: no pool
 static_assert(DB_STAGES >= 2 && DB_STAGES <= 16, "stage ring size");
 
 // bf16 dispatch through bulk copies.  Each CTA is one warp driving one
@@ -55,8 +54,10 @@ static_assert(DB_STAGES >= 2 && DB_STAGES <= 16, "stage ring size");
 //
 // Units: each CTA first takes `per_cta` consecutive units of its own, then
 // draws `grab` consecutive units at a time from the pool of the rest (the
-// scheduling slot `sched_slot` of the launch; see sched.cuh).  The stage ring
-// records the unit each stage holds.
+// scheduling slot `sched_slot` of the launch; see sched.cuh).  With
+// sched_slot < 0 there is no pool: CTA b takes units [units*b/G,
+// units*(b+1)/G) of G CTAs.  The stage ring records the unit each stage
+// holds.
 //
 // COAL: rows go to the rank-coalesced buffer (one row per token and distinct
 // destination rank).  slot_of is then the coalesced row map, where every slot
@@ -94,9 +95,11 @@ __global__ void __launch_bounds__(32)
     // the unit source (warp-uniform): this CTA's range, then draws from the
     // pool [per_cta * gridDim.x, units); a draw is requested as soon as the
     // current range is used up, so it travels while the last unit loads
-    SchedSlot *sched = g_dispatch_sched + sched_slot;
-    const int64_t pool0 = per_cta * gridDim.x;
-    int64_t r_cur = per_cta * blockIdx.x, r_end = r_cur + per_cta;
+    const bool pooled = sched_slot >= 0;
+    SchedSlot *sched = g_dispatch_sched + (pooled ? sched_slot : 0);
+    const int64_t pool0 = pooled ? per_cta * gridDim.x : units;
+    int64_t r_cur = pooled ? per_cta * blockIdx.x : units * blockIdx.x / gridDim.x;
+    int64_t r_end = pooled ? r_cur + per_cta : units * (blockIdx.x + 1) / gridDim.x;
     unsigned long long drawn = 0;  // lane 0: the pending draw's pool offset
     bool pending = false, dry = pool0 >= units;
     auto request = [&]() {
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(32)
             (void)mbar_wait(full((int)(m % DB_STAGES)), (uint32_t)(m / DB_STAGES) & 1);
     }
     bulk_wait_all();
-    if (lane == 0)
+    if (pooled && lane == 0)
         sched_finish(sched);
 }
 
@@ -287,11 +290,13 @@ static cudaError_t launch_dispatch_bulk(int T, int H, int k, const void *x,
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const int64_t g = units < cap ? units : cap;
     const int64_t even = units / g;
-    const int64_t per_cta = even >= DB_DYN_MIN ? units * DB_STATIC_PCT / 100 / g : even;
+    const bool pooled = even >= DB_DYN_MIN;
+    const int64_t per_cta = pooled ? units * DB_STATIC_PCT / 100 / g : 0;
     return launch_pdl(dispatch_bulk_kernel<COAL>, dim3((unsigned)g), dim3(32), smem, stream,
                       static_cast<const uint8_t *>(x), slot_of, static_cast<uint8_t *>(recv), T, k,
                       rowbytes, CH, nchunks, units, per_cta, DB_GRAB,
-                      next_sched_slot(g_dispatch_seq), rows, prefetch_x ? 1 : 0, err_word);
+                      pooled ? next_sched_slot(g_dispatch_seq) : -1, rows, prefetch_x ? 1 : 0,
+                      err_word);
 }
 
 cudaError_t launch_dispatch_coalesced(int T, int H, int k, const void *x, const int32_t *crow,

@@ -4,7 +4,8 @@ share, then draws the rest from a counter of the launch): every unit is copied
 on shapes that take the fixed share by percentage and by the whole units of
 an equal split; the counter's slot is clean again for the next launch, for
 the replays of a captured graph, and after more launches than there are
-slots, from two streams at once.  Each receive buffer is compared bit for bit
+slots, from two streams at once.  Launches with few units per CTA take a
+static split instead (no pool).  Each receive buffer is compared bit for bit
 with the oracle's dispatch."""
 import numpy as np
 import pytest
@@ -30,10 +31,11 @@ def _case(seed, T, H, k, E):
     return w, slot_of
 
 
-# (T, H, k, E): 8192 one-chunk rows (about 9 units per CTA: half of them drawn);
-# 3000 rows of two unequal chunks (about 6.6 units per CTA: the remainder of
-# an equal split drawn); 911 single units (fewer units than CTAs could run)
-SHAPES = [(8192, 256, 4, 32), (3000, 7168, 3, 24), (911, 64, 2, 8)]
+# (T, H, k, E): 8192 one-chunk rows (about 9 units per CTA: half of them
+# drawn); 20000 rows of two unequal chunks (44 units per CTA); 3000 rows of two
+# chunks (about 6.6 units per CTA: a static split, no pool); 911 single units
+# (fewer units than CTAs could run)
+SHAPES = [(8192, 256, 4, 32), (20000, 7168, 1, 4), (3000, 7168, 3, 24), (911, 64, 2, 8)]
 
 
 @pytest.mark.parametrize("T,H,k,E", SHAPES)
@@ -84,7 +86,7 @@ def test_more_launches_than_slots_on_two_streams():
     launches free to overlap; each stream's buffer is checked every 100
     launches and at the end."""
     import combine_layout_moe_gb300 as m
-    T, H, k, E = 2048, 64, 2, 8
+    T, H, k, E = 8192, 64, 2, 8    # about 9 units per CTA: the pool
     cases = [_case(40 + i, T, H, k, E) for i in range(2)]
     streams = [torch.cuda.Stream() for _ in range(2)]
     errs = [m.new_error_word() for _ in range(2)]
