@@ -24,6 +24,14 @@
  *     moe_read_error() synchronises the stream and reports it.  Outputs are
  *     undefined after any error.
  *   - A failed CUDA launch returns MOE_ERR_CUDA.
+ *   - The dispatch kernels share large launches out at run time: each CTA (or
+ *     warp) takes a fixed part of the work and draws the rest from a counter
+ *     of the launch.  The counters live in a table of 1024 slots per kernel
+ *     family in the library's own device memory (static, allocated when the
+ *     library loads); a launch takes the next slot and its last CTA clears
+ *     it.  Launches of one family may run concurrently, and a captured CUDA
+ *     graph may be replayed, as long as fewer than 1024 of them execute at
+ *     the same moment on one device.
  */
 #ifndef MOE_EP_H
 #define MOE_EP_H
