@@ -1,12 +1,13 @@
-// Dynamic tail for the bulk dispatch (sm_103a).
+// Dynamic tail for the dispatch kernels (sm_103a).
 //
-// A static split gives each CTA an equal contiguous range of units, but the
-// CTAs of one launch do not move bytes at equal rates: six one-warp CTAs
-// share each SM, and on GB300 their rates differ by more than half between
-// the slowest and the fastest tenth, so a static split ends when the slowest
-// CTA ends while the SMs of the others idle.  Each CTA therefore takes a
-// fixed share of the units as its own range and then draws the rest, a few
-// at a time, from a pool shared by the launch: CTAs that run ahead take more.
+// A static split gives each CTA (or warp) an equal share of the units, but
+// the CTAs of one launch do not move bytes at equal rates: six one-warp CTAs
+// of the bulk dispatch share each SM, and on GB300 their rates differ by more
+// than half between the slowest and the fastest tenth, so a static split
+// ends when the slowest CTA ends while the SMs of the others idle.  Each CTA
+// (bulk dispatch) or warp (FP8 dispatch) therefore takes a fixed part of the
+// work as its own and then draws the rest, a few units at a time, from a pool
+// shared by the launch: those that run ahead take more.
 //
 // The pool counter lives in a slot of a file-scope table in device memory
 // (the library allocates nothing per call).  The host hands out slots round
