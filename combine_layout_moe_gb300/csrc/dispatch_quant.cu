@@ -7,10 +7,11 @@
 // nearest-even conversion.  The token is quantised once and the same codes
 // and scales go to all k slots (or, COAL, once per coalesced row).
 //
-// GPU design: a warp item is one token and 2U blocks of 128 channels; each
-// half-warp owns a block (16 lanes x 8 channels, U 16-byte vectors of x in
-// flight per lane), reduces its amax with xor-shuffles, and stores 8-byte code
-// words and one fp32 scale per block to every destination row.  When the
+// GPU design: a warp item is one token and 2U blocks of 128 channels (U
+// 16-byte vectors of x in flight per lane, in adjacent pairs); eight lanes own
+// a block (8 lanes x 16 channels), reduce its amax with xor-shuffles, and
+// store 16-byte code words and one fp32 scale per block to every destination
+// row.  When the
 // items take more than QUANT_DYN_MIN_ROUNDS rounds of the resident warps, the
 // warps take QUANT_STATIC_PCT percent of them in interleaved rounds (warp w:
 // items w, w + warps, ...), then draw the rest from the launch's pool
@@ -58,10 +59,12 @@ constexpr int QUANT_DYN_MIN_ROUNDS = MOE_QUANT_DYN_MIN_ROUNDS;
 __device__ SchedSlot g_quant_sched[SCHED_SLOTS];
 static std::atomic<unsigned> g_quant_seq{0};
 
-// FP8: each half-warp owns one 128-channel block (16 lanes x 8 channels).
-// The amax is reduced with xor-shuffles inside the half-warp; scale and
-// reciprocal are each one correctly rounded fp32 division; each channel is one
-// rounded fp32 multiply followed by a saturating nearest-even E4M3 conversion.
+// FP8: eight lanes own one 128-channel block (8 lanes x 16 channels: two
+// adjacent 16-byte vectors of x, whose 16 codes go out in one 16-byte store
+// per slot).  The amax is reduced with xor-shuffles inside the eight lanes;
+// scale and reciprocal are each one correctly rounded fp32 division; each
+// channel is one rounded fp32 multiply followed by a saturating nearest-even
+// E4M3 conversion.
 template <int U, bool COAL, bool POOL>
 __global__ void __launch_bounds__(QUANT_THREADS)
     dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ slot_of,
@@ -69,6 +72,8 @@ __global__ void __launch_bounds__(QUANT_THREADS)
                         int H, int groups, int64_t items, int64_t pool_from, int grab,
                         int sched_slot, int N, int prefetch_x, uint32_t *err_word)
 {
+    static_assert(U % 2 == 0, "vectors go in adjacent pairs");
+    constexpr int P = U / 2;  // vector pairs per lane per item
     // POOL: items from pool_from on are drawn; else every item is taken in
     // interleaved rounds and the pool code is compiled out
     const int64_t static_items = POOL ? pool_from : items;
@@ -125,30 +130,37 @@ __global__ void __launch_bounds__(QUANT_THREADS)
             static_items < items)
             request();
         const int64_t t = it / groups;
-        const int c0 = (int)(it - t * groups) * (32 * U) + lane;
+        // lane `lane` holds pairs of adjacent vectors (16 channels): pair p is
+        // vectors base + 64p + 2 lane + {0, 1}; eight lanes cover a block
+        const int base = (int)(it - t * groups) * (32 * U);
         const uint4 *src = x + t * C;
         uint4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            v[u] = c0 + u * 32 < C ? ld_stream_v4(src + c0 + u * 32) : make_uint4(0, 0, 0, 0);
+        for (int p = 0; p < P; ++p) {
+            const int c = base + 64 * p + 2 * lane;
+            const bool in = c < C;  // C is a multiple of 16: a pair is whole or absent
+            v[2 * p] = in ? ld_stream_v4(src + c) : make_uint4(0, 0, 0, 0);
+            v[2 * p + 1] = in ? ld_stream_v4(src + c + 1) : make_uint4(0, 0, 0, 0);
+        }
 
-        uint2 code[U];
-        float scale[U];
+        uint4 code[P];
+        float scale[P];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            float f[8];
+        for (int p = 0; p < P; ++p) {
+            const uint32_t w[8] = {v[2 * p].x,     v[2 * p].y,     v[2 * p].z,     v[2 * p].w,
+                                   v[2 * p + 1].x, v[2 * p + 1].y, v[2 * p + 1].z, v[2 * p + 1].w};
+            float f[16];
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                f[2 * p] = bf16lo(w[p]);
-                f[2 * p + 1] = bf16hi(w[p]);
+            for (int q = 0; q < 8; ++q) {
+                f[2 * q] = bf16lo(w[q]);
+                f[2 * q + 1] = bf16hi(w[q]);
             }
             float amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 16; ++i)
                 amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
-            for (int o = 8; o >= 1; o >>= 1)
+            for (int o = 4; o >= 1; o >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, o));
             bool zero = !(amax > 0.0f);
             float inv = 0.0f, sc = 1.0f;
@@ -159,26 +171,26 @@ __global__ void __launch_bounds__(QUANT_THREADS)
                 else
                     sc = __fdiv_rn(amax, 448.0f);
             }
-            uint32_t packed[2];
+            uint32_t packed[4];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < 4; ++h) {  // code word h: channels 4h .. 4h+3
                 uint32_t word = 0;
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const int i = 4 * h + 2 * p;
+                for (int q = 0; q < 2; ++q) {
+                    const int i = 4 * h + 2 * q;
                     uint32_t pair;
                     if (zero) {
-                        const uint32_t src_w = w[2 * h + p];
+                        const uint32_t src_w = w[2 * h + q];
                         pair = ((src_w >> 15) & 1u) << 7 | ((src_w >> 31) & 1u) << 15;
                     } else {
                         pair = e4m3x2(__fmul_rn(f[i], inv), __fmul_rn(f[i + 1], inv));
                     }
-                    word |= (pair & 0xffffu) << (16 * p);
+                    word |= (pair & 0xffffu) << (16 * q);
                 }
                 packed[h] = word;
             }
-            code[u] = make_uint2(packed[0], packed[1]);
-            scale[u] = sc;
+            code[p] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            scale[p] = sc;
         }
 
         if (!waited) {
@@ -209,12 +221,12 @@ __global__ void __launch_bounds__(QUANT_THREADS)
                 uint8_t *dq = recv_q + (int64_t)s * H;
                 float *ds = recv_scales + (int64_t)s * B;
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = c0 + u * 32;
+                for (int p = 0; p < P; ++p) {
+                    const int c = base + 64 * p + 2 * lane;
                     if (c < C) {
-                        st_v2(dq + (int64_t)c * 8, code[u]);
-                        if ((lane & 15) == 0)
-                            ds[c >> 4] = scale[u];
+                        st_v4(dq + (int64_t)c * 8, code[p]);
+                        if ((lane & 7) == 0)
+                            ds[c >> 4] = scale[p];
                     }
                 }
             }
