@@ -209,3 +209,38 @@ def test_fp8_exchange_over_gloo_matches_oracle(W, T_per, H, k, E):
         assert np.array_equal(g_s, ts[tok])
         assert np.array_equal(g_offs, np.concatenate([[0], np.cumsum(counts[d].sum(axis=0))]))
         assert np.array_equal(g_out.reshape(outs[d].shape), outs[d])
+
+
+def test_virtual_step_fp8_needs_an_expert():
+    """The FP8 receive buffers are (codes, scales) pairs: without an expert
+    returning bf16 rows there is nothing to send back."""
+    from combine_layout_moe_gb300 import ep
+    ins = _inputs(2, [4, 4], 128, 2, 4)
+    with pytest.raises(ValueError):
+        ep.virtual_step([_bf16(w.x) for w in ins], [torch.from_numpy(w.topk_idx) for w in ins],
+                        [torch.from_numpy(w.topk_w) for w in ins], 4, ops=CpuOps(), quant=True)
+
+
+@pytest.mark.parametrize("T_per", [[13], [0]])
+def test_single_rank_is_the_local_path(T_per):
+    """W = 1: the exchange is the identity and the receive order is the
+    rank's own dispatch order; empty batches pass through."""
+    from combine_layout_moe_gb300 import ep
+    H, k, E = 8, 3, 5
+    ins = _inputs(1, T_per, H, k, E)
+    ys = {}
+
+    def expert(recv, offs):
+        ys[0] = expert_output(recv.shape[0], H, seed=710)
+        return _bf16(ys[0])
+
+    recv, offs, outs = ep.virtual_step([_bf16(ins[0].x)], [torch.from_numpy(ins[0].topk_idx)],
+                                       [torch.from_numpy(ins[0].topk_w)], E, expert=expert,
+                                       ops=CpuOps())
+    _, o_recv, _ = oracle.ep_dispatch([ins[0].topk_idx], [ins[0].x], E)
+    assert np.array_equal(_bits(recv[0]).reshape(o_recv[0].shape), o_recv[0])
+    # one rank: the expert-major receive order is the layout's own slot order
+    assert np.array_equal(o_recv[0], oracle.dispatch(ins[0].x, oracle.layout(ins[0].topk_idx, E, 1)[3]))
+    o_out = oracle.ep_combine([ins[0].topk_idx], [ins[0].topk_w], [ys[0]], E)
+    assert np.array_equal(_bits(outs[0]).reshape(o_out[0].shape), o_out[0])
+    assert offs[0].tolist() == [0] + np.cumsum(np.bincount(ins[0].topk_idx.ravel(), minlength=E)).tolist()
